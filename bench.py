@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Benchmark of the bitwise-aligned causal GQA attention hot path on GB300.
+
+One step = one causal prefill (B=4, S=16384) and one one-token decode
+(B=16, ctx=8192), Hq=32, Hkv=8, D=128, bf16, through the library's C ABI.
+Inputs are synthetic (iid N(0,1) rounded to bf16, seeded) and larger than L2.
+
+Prints ONE JSON line.  `value` is prefill throughput in causal TFLOP/s
+(4*B*Hq*D*S(S+1)/2 per call) summed over ranks; the decode leg's KV GB/s sits
+under "decode".  `--impl reference` times the fp64 CPU oracle instead, on a
+bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
+For N>1 launch one process per GPU with torch.distributed.run.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill causal TFLOP/s & decode KV GB/s at 1 GB300 (% roofline), bitwise-aligned"
+HQ, HKV, D = 32, 8, 128
+# full: the headline workload; small: the same kernels at a size an ncu
+# replay handles quickly (inputs still larger than L2)
+WORKLOADS = {"full": (4, 16384, 16, 8192), "small": (4, 4096, 16, 8192)}
+PREFILL_B, PREFILL_S, DECODE_B, DECODE_CTX = WORKLOADS["full"]
+SEED_PREFILL = 7_000_001
+SEED_DECODE = 7_000_002
+
+
+def workload_name():
+    return (f"causal GQA prefill B={PREFILL_B} S={PREFILL_S} + one-token decode B={DECODE_B} ctx={DECODE_CTX}, "
+            f"Hq={HQ} Hkv={HKV} D={D} bf16")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# ncu dram bytes per launch for the current kernels (profiles/ summaries); None = not captured
+NCU_TRAFFIC_BYTES = {"prefill": None, "decode": None}
+
+
+def prefill_flops(B: int, S: int) -> int:
+    """Algorithmic causal FLOPs: Q K^T and P V over the S(S+1)/2 visible pairs."""
+    return 4 * B * HQ * D * S * (S + 1) // 2
+
+
+def decode_bytes(B: int, ctx: int) -> int:
+    """Algorithmic bytes: K and V of the context read once per KV head, q read and o written."""
+    return 2 * B * HKV * ctx * D * 2 + 2 * B * HQ * D * 2
+
+
+# ------------------------------------------------------------------ environment
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                raw = json.load(f)
+            flat = {}
+
+            def walk(d):
+                for kk, vv in d.items():
+                    if isinstance(vv, dict):
+                        walk(vv)
+                    elif isinstance(vv, (int, float)):
+                        flat.setdefault(kk, float(vv))
+
+            walk(raw)
+            if "hbm_gbs" in flat and "bf16_tflops" in flat:
+                out = {"hbm_gbs": flat["hbm_gbs"], "bf16_tflops": flat["bf16_tflops"],
+                       "bf16_tflops_sustained": flat.get("bf16_tflops_sustained", flat["bf16_tflops"]),
+                       "source": "measured"}
+                return out
+        except Exception:  # noqa: BLE001 - fall through to the fallback figures
+            pass
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="kb_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ distributed glue
+
+def dist_setup(n_gpus: int):
+    """(rank, world, local_rank) -- one process per GPU under torch.distributed.run."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if n_gpus > 1 and world != n_gpus:
+        raise SystemExit(f"--gpus {n_gpus} needs a torch.distributed.run launch with {n_gpus} processes")
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = os.environ.get("KB_DIST_BACKEND", "nccl")
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+
+        if dist.get_backend() == "nccl" and device is not None:
+            dist.barrier(device_ids=[device])
+        else:
+            dist.barrier()
+
+
+def reduce_max(value: float, world: int, device: str = "cpu") -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_units: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: every rank processed `per_rank_units`; the job took the slowest rank's time."""
+    return per_rank_units * world / max_seconds
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+
+def oracle_sample_rate(x_pre, budget_s: float, seed: int, n_threads: int | None = None):
+    """Time the oracle on random prefill rows of the workload for ~budget_s; return (flop/s, rows, threads)."""
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    B, _, S, _ = x_pre.q.shape
+    nt = oracle.default_threads() if n_threads is None else n_threads
+    flops = 0
+    rows_done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        n = max(nt, 32)
+        rows = np.stack([rng.integers(0, B, n), rng.integers(0, HQ, n), rng.integers(0, S, n)], axis=1)
+        oracle.attention_rows(x_pre.q, x_pre.k, x_pre.v, rows, n_threads=nt)
+        flops += int(sum(4 * D * (int(i) + 1) for i in rows[:, 2]))
+        rows_done += n
+    dt = time.perf_counter() - t0
+    return flops / dt, rows_done, nt, dt
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    from bitwise_aligned_causal_gb300 import inputs
+
+    x = inputs.make_qkv(PREFILL_B, PREFILL_S, SEED_PREFILL)
+    for _ in range(args.warmup):
+        oracle_sample_rate(x, 0.5, seed=11)
+    rates, secs, rows, nt = [], [], 0, 1
+    for s in range(args.steps):
+        r, n, nt, dt = oracle_sample_rate(x, 2.0, seed=100 + s)
+        rates.append(r)
+        secs.append(dt)
+        rows += n
+    value = statistics.mean(rates) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: iid N(0,1) rounded to bf16 (numpy default_rng)",
+        "config": {"workload": workload_name(), "parallelism": "none (CPU oracle, rank 0 only)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
+                         "sample": f"{rows} random prefill query rows of the workload (about 2 s of oracle work per step)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    from bitwise_aligned_causal_gb300 import build, inputs
+
+    torch.cuda.set_device(local)
+    build.build()
+    from bitwise_aligned_causal_gb300 import kb_attn
+
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    x = inputs.make_qkv(PREFILL_B, PREFILL_S, SEED_PREFILL + 1000 * rank)
+    y = inputs.make_qkv(DECODE_B, DECODE_CTX, SEED_DECODE + 1000 * rank, Lq=1)
+    q, k, v = to_dev(x.q), to_dev(x.k), to_dev(x.v)
+    qd, kd, vd = to_dev(y.q), to_dev(y.k), to_dev(y.v)
+    o = torch.empty_like(q)
+    od = torch.empty_like(qd)
+
+    def step():
+        kb_attn.prefill(q, k, v, out=o)
+        kb_attn.decode(qd, kd, vd, DECODE_CTX, out=od)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    kb_attn.check_device_status()
+
+    # --- timed region: device-resident inputs, events per kernel on the launching stream
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    barrier(world, local)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(n):
+            ev[i][0].record(stream)
+            kb_attn.prefill(q, k, v, out=o)
+            ev[i][1].record(stream)
+            kb_attn.decode(qd, kd, vd, DECODE_CTX, out=od)
+            ev[i][2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world, local)
+    clocks = clk.summary()
+    kb_attn.check_device_status()
+    total_ms = t_start.elapsed_time(t_end)
+    pre_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    step_ms_max = reduce_max(total_ms / n, world, "cuda" if world > 1 else "cpu")
+    pre_ms_max = reduce_max(pre_ms, world, "cuda" if world > 1 else "cpu")
+    dec_ms_max = reduce_max(dec_ms, world, "cuda" if world > 1 else "cpu")
+
+    pf = prefill_flops(PREFILL_B, PREFILL_S)
+    db = decode_bytes(DECODE_B, DECODE_CTX)
+    pre_tflops = aggregate(pf, world, pre_ms_max / 1e3) / 1e12
+    dec_gbs = aggregate(db, world, dec_ms_max / 1e3) / 1e9
+
+    # --- end to end: pinned host inputs copied in, result copied out, every step
+    if args.no_e2e:
+        e2e = None
+    else:
+        e2e = run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_attn)
+    if rank != 0:
+        return
+    emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks, x)
+
+
+def run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_attn):
+    import numpy as np
+    import torch
+
+    n = args.steps
+    pf = prefill_flops(PREFILL_B, PREFILL_S)
+    db = decode_bytes(DECODE_B, DECODE_CTX)
+    hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+                  for a in (x.q, x.k, x.v))
+    hqd, hkd, hvd = (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+                     for a in (y.q, y.k, y.v))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hod = torch.empty(od.shape, dtype=od.dtype).pin_memory()
+    h2d = sum(t.numel() * 2 for t in (hq, hk, hv, hqd, hkd, hvd))
+    d2h = (ho.numel() + hod.numel()) * 2
+    e2e_n = max(1, min(n, 10))
+    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e2e_n)]
+    barrier(world, local)
+    torch.cuda.synchronize()
+    for i in range(e2e_n):
+        ee[i][0].record(stream)
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        kb_attn.prefill(q, k, v, out=o)
+        ho.copy_(o, non_blocking=True)
+        ee[i][1].record(stream)
+        qd.copy_(hqd, non_blocking=True)
+        kd.copy_(hkd, non_blocking=True)
+        vd.copy_(hvd, non_blocking=True)
+        kb_attn.decode(qd, kd, vd, DECODE_CTX, out=od)
+        hod.copy_(od, non_blocking=True)
+        ee[i][2].record(stream)
+    torch.cuda.synchronize()
+    kb_attn.check_device_status()
+    e2e_pre_ms = reduce_max(statistics.mean(e[0].elapsed_time(e[1]) for e in ee), world,
+                            "cuda" if world > 1 else "cpu")
+    e2e_dec_ms = reduce_max(statistics.mean(e[1].elapsed_time(e[2]) for e in ee), world,
+                            "cuda" if world > 1 else "cpu")
+    return {"value": aggregate(pf, world, e2e_pre_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "decode_gbs": aggregate(db, world, e2e_dec_ms / 1e3) / 1e9,
+            "note": "pinned host buffers copied in and results copied out inside every timed step"}
+
+
+def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks,
+              x):
+    pf = prefill_flops(PREFILL_B, PREFILL_S)
+    db = decode_bytes(DECODE_B, DECODE_CTX)
+    peaks = load_peaks()
+    pre_per_launch = pf / (pre_ms / 1e3) / 1e12
+    dec_per_launch = db / (dec_ms / 1e3) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, rows, nt, dt = oracle_sample_rate(x, args.cpu_seconds, seed=99)
+        cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
+               "sample": f"{rows} random prefill query rows of the workload, {dt:.1f} s of oracle work on "
+                         f"{os.cpu_count()} host cores"}
+    tr_pre = NCU_TRAFFIC_BYTES["prefill"]
+    tr_dec = NCU_TRAFFIC_BYTES["decode"]
+    line = {
+        "metric": METRIC,
+        "value": pre_tflops,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": n,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": step_ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: iid N(0,1) rounded to bf16 (numpy default_rng, seeds 7000001/7000002 + 1000*rank)",
+        "config": {
+            "workload": workload_name(),
+            "prefill": {"B": PREFILL_B, "S": PREFILL_S, "Hq": HQ, "Hkv": HKV, "D": D},
+            "decode": {"B": DECODE_B, "ctx": DECODE_CTX, "Hq": HQ, "Hkv": HKV, "D": D},
+            "parallelism": f"replicas x{world} (independent batches per GPU)",
+            "l2": (f"inputs larger than L2 (prefill q/k/v {3 * PREFILL_B * HQ * PREFILL_S * D * 2 // 2 // 1000000} MB, "
+                   f"decode K/V {2 * DECODE_B * HKV * DECODE_CTX * D * 2 // 1000000} MB per step), no flush"),
+        },
+        "decode": {
+            "value": dec_gbs, "unit": "GB/s", "ms": dec_ms_max,
+            "roofline": {"bound": "hbm", "achieved": dec_per_launch, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": dec_per_launch / peaks["hbm_gbs"],
+                         "traffic": tr_dec, "peak_source": peaks["source"]},
+        },
+        "roofline": {
+            "bound": "tensor", "achieved": pre_per_launch, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": pre_per_launch / peaks["bf16_tflops"], "traffic": tr_pre,
+            "kernel": "kb_prefill_kernel", "peak_source": peaks["source"] + " burst bf16",
+            "frac_of_sustained": pre_per_launch / peaks["bf16_tflops_sustained"],
+        },
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * n,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="full")
+    args = ap.parse_args()
+    global PREFILL_B, PREFILL_S, DECODE_B, DECODE_CTX
+    PREFILL_B, PREFILL_S, DECODE_B, DECODE_CTX = WORKLOADS[args.workload]
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,161 @@
+// kb_contract.cuh -- the numerical contract shared by every entry point.
+//
+// The KernelBraid README ("Method") requires one numerical contract that
+// connects full-sequence prefill, partitioned (chunked) forward and
+// one-token decode, so that the three produce bitwise-identical output rows
+// for the same inputs and context ("Advantages"; the "Usage" example compares
+// the raw bf16 bits).  The pages do not print the contract's contents, so it
+// is fixed here, version 1:
+//
+//  C1 One KV tile of 128 keys, anchored at key 0, visited in ascending order
+//     0..floor(p/128) for a row at absolute position p.  Prefill/chunk query
+//     tiles are aligned to absolute multiples of 128, so every row of a tile
+//     ends on the same KV tile and no row ever visits a fully masked tile.
+//  C2 One MMA: tcgen05.mma.cta_group::1.kind::f16, bf16 x bf16 -> fp32,
+//     M=128 N=128 K=16.  S = Q K^T and O += P V each issue eight of them in
+//     ascending K order; S is A/B from shared memory, P V reads P from TMEM.
+//  C3 One thread owns one row of S and O (TMEM lane = row).  All row math is
+//     the functions below; data-dependent choices are per row only.
+//  C4 One normalisation: o = bf16_rn(O * rcp_rn(l)).
+//  C5 No split of the KV range (a split would be a fixed, length-determined
+//     partition folded identically by every entry point).
+//
+// Every floating-point operation below is an explicit round-to-nearest
+// intrinsic, so the compiler cannot contract or reorder them differently in
+// different kernels.
+#pragma once
+
+#include <cstdint>
+#include "kb_ptx.cuh"
+
+namespace kb {
+
+constexpr int kHeadDim = 128;      // D
+constexpr int kTileKeys = 128;     // keys per KV tile (C1)
+constexpr int kTileRows = 128;     // query rows per tile = MMA M (C2)
+constexpr int kGroup = 4;          // query heads per KV head (32 / 8)
+constexpr int kContractVersion = 1;
+
+// c = log2(e) / sqrt(128) = 0.1275174308245986852... rounded to the nearest
+// fp32, bit pattern 0x3E0293EE.  The softmax weight of score s against the
+// running max m is 2^(s*c - m*c) = e^((s - m) / sqrt(128)).
+constexpr uint32_t kScoreScaleLog2Bits = 0x3E0293EEu;
+__device__ __forceinline__ float score_scale_log2() { return __uint_as_float(kScoreScaleLog2Bits); }
+
+constexpr uint32_t kTileBytes = kTileRows * kHeadDim * 2;   // one bf16 128x128 tile
+constexpr uint32_t kSlabBytes = kTileBytes / 2;             // one 128 x 64 swizzled slab
+
+// Instruction descriptors for the two products (C2).
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0);  // B = K tile, K-major
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 1);  // B = V tile, MN-major
+
+// Descriptor of k-step kk (0..7) of a K-major 128-row tile stored as two
+// 128-byte-swizzled slabs (d 0..63, d 64..127).  `sbo` is the distance
+// between 8-row groups: 1024 for a full tile, 0 when all row groups alias one
+// 8-row atom (decode, where only rows 0..3 carry queries).
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_saddr, int kk, uint32_t sbo, uint32_t slab_bytes) {
+  const uint32_t a = tile_saddr + static_cast<uint32_t>(kk >> 2) * slab_bytes + static_cast<uint32_t>(kk & 3) * 32u;
+  return smem_desc_sw128(a, 16u, sbo);
+}
+
+// Descriptor of k-step kk (keys 16kk..16kk+15) of a V tile: keys are rows,
+// d is contiguous (MN-major), slabs of 64 d-columns 16 KB apart.
+__device__ __forceinline__ uint64_t desc_v(uint32_t tile_saddr, int kk) {
+  return smem_desc_sw128(tile_saddr + static_cast<uint32_t>(kk) * 2048u, kSlabBytes, 1024u);
+}
+
+// Issue S = Q K^T for one query tile (C2: eight K=16 steps, ascending).
+__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint32_t q_saddr, uint32_t q_sbo, uint32_t q_slab,
+                                         uint32_t k_saddr) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ss(s_tmem, desc_kmajor(q_saddr, kk, q_sbo, q_slab), desc_kmajor(k_saddr, kk, 1024u, kSlabBytes), kIdescQK,
+           kk > 0 ? 1u : 0u);
+}
+
+// Issue O (+)= P V (C2).  P sits in TMEM as bf16 pairs, 8 columns per K step.
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_saddr, bool first_tile) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts(o_tmem, p_tmem + static_cast<uint32_t>(kk) * 8u, desc_v(v_saddr, kk), kIdescPV,
+           (first_tile && kk == 0) ? 0u : 1u);
+}
+
+// Per-row running state of the online softmax.
+struct RowState {
+  float m;  // running max of the raw scores q.k (unscaled)
+  float l;  // running sum of the fp32 weights
+};
+
+__device__ __forceinline__ RowState row_state_init() { return RowState{-INFINITY, 0.0f}; }
+
+// One KV tile of the online softmax for one row (C3).
+//
+//  s[k]     raw scores q.k of keys 128j+k (fp32 bit patterns from TMEM)
+//  n_valid  number of visible keys in this tile (keys >= n_valid are masked);
+//           128 except on the row's last tile
+//  p        out: the weights rounded to bf16, packed two per word, key 2i in
+//           the low half of p[i]
+//  returns  alpha, the factor the row's O accumulator must be scaled by
+//           before this tile's P V is added (exactly 1.0 when the max did not
+//           change, exactly 0.0 on the first tile)
+//
+//  m'    = max(m, max_k s[k])                          (exact)
+//  mc    = m' * c                                      (c = log2(e)/sqrt(128))
+//  alpha = 1 if m' == m else 2^(fma(m, c, -mc))
+//  w[k]  = 2^(fma(s[k], c, -mc)),  masked keys -> +0
+//  l'    = fma(l, alpha, sum_k w[k]) with the sum taken as eight strided
+//          partial sums (k mod 8, ascending k) combined as a balanced tree
+__device__ __forceinline__ float row_softmax_tile(const uint32_t (&s)[128], int n_valid, RowState& st,
+                                                  uint32_t (&p)[64]) {
+  const float c = score_scale_log2();
+  float x[128];
+#pragma unroll
+  for (int k = 0; k < 128; ++k) x[k] = (k < n_valid) ? __uint_as_float(s[k]) : -INFINITY;
+
+  float mx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mx[i] = x[i];
+#pragma unroll
+  for (int k = 8; k < 128; ++k) mx[k & 7] = fmaxf(mx[k & 7], x[k]);
+  const float tile_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  const float m_new = fmaxf(st.m, tile_max);
+  const float mc = __fmul_rn(m_new, c);
+  const float neg_mc = -mc;
+  const float alpha = (m_new == st.m) ? 1.0f : ex2_approx(__fmaf_rn(st.m, c, neg_mc));
+
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 128; ++k) {
+    const float w = ex2_approx(__fmaf_rn(x[k], c, neg_mc));
+    x[k] = w;
+    if (k < 8) acc[k] = w;
+    else acc[k & 7] = __fadd_rn(acc[k & 7], w);
+  }
+  const float tile_sum = __fadd_rn(__fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3])),
+                                   __fadd_rn(__fadd_rn(acc[4], acc[5]), __fadd_rn(acc[6], acc[7])));
+#pragma unroll
+  for (int i = 0; i < 64; ++i) p[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+
+  st.l = __fmaf_rn(st.l, alpha, tile_sum);
+  st.m = m_new;
+  return alpha;
+}
+
+// Scale 32 accumulator columns by alpha (bit-neutral when alpha == 1).
+__device__ __forceinline__ void rescale32(uint32_t (&o)[32], float alpha) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__fmul_rn(__uint_as_float(o[i]), alpha));
+}
+
+// C4: final normalisation of 32 accumulator columns into 16 bf16 pairs.
+__device__ __forceinline__ void normalise32(const uint32_t (&o)[32], float inv_l, uint32_t (&out)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    out[i] = pack_bf16x2(__fmul_rn(__uint_as_float(o[2 * i]), inv_l), __fmul_rn(__uint_as_float(o[2 * i + 1]), inv_l));
+}
+
+__device__ __forceinline__ float row_inv_l(const RowState& st) { return __frcp_rn(st.l); }
+
+}  // namespace kb

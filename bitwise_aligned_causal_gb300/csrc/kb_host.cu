@@ -1,0 +1,240 @@
+// kb_host.cu -- the C ABI of libkb_attn.so: argument checks, TMA tensor-map
+// encoding and kernel launches.  Declarations and their contract are in
+// include/kb_attn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/kb_attn.h"
+#include "kb_contract.cuh"
+#include "kb_launch.h"
+
+namespace {
+
+constexpr int kMaxRows = 1 << 22;     // positions per sequence (4M)
+constexpr int kMaxDevices = 64;
+
+// Device error word (0 = fine).  Kernels get its address as an argument.
+__device__ uint32_t g_kb_error_word;
+
+struct DeviceState {
+  uint32_t* err = nullptr;
+  bool ready = false;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+kb_status get_device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KB_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return KB_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_kb_error_word) != cudaSuccess) return KB_ERR_CUDA;
+    st.err = static_cast<uint32_t*>(p);
+    st.ready = true;
+  }
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q{};
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return KB_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = &st;
+  return KB_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The pointer must be device (or managed) memory reachable from the current device.
+kb_status check_device_pointer(const void* p) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return KB_ERR_INVALID_ARG;
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return KB_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KB_ERR_CUDA;
+  if (attr.type == cudaMemoryTypeDevice && attr.device != dev) return KB_ERR_INVALID_ARG;
+  return KB_OK;
+}
+
+// Rows of 128 bf16, box of 64 columns x 128 rows, 128-byte swizzle.
+// `rows` rows are in bounds in each of `planes` planes `plane_stride` bytes
+// apart; reads beyond `rows` are zero-filled by the TMA unit.
+kb_status encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes, uint64_t plane_stride) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kb::kHeadDim), rows, planes};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kb::kHeadDim) * 2u, plane_stride};
+  cuuint32_t box[3] = {64u, 128u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KB_OK : KB_ERR_CUDA;
+}
+
+kb_status check_heads(int B, int Hq, int Hkv) {
+  if (B < 1 || Hq < 1 || Hkv < 1) return KB_ERR_INVALID_ARG;
+  if (Hq != kb::kGroup * Hkv) return KB_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq > (1LL << 24)) return KB_ERR_UNSUPPORTED;
+  return KB_OK;
+}
+
+kb_status check_ptrs(const void* q, const void* k, const void* v, const void* o) {
+  if (!q || !k || !v || !o) return KB_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return KB_ERR_INVALID_ARG;
+  return KB_OK;
+}
+
+kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int L, int start,
+                     int kv_cap, int q_tiles_per_cta, void* stream) {
+  kb_status s = check_ptrs(q, k, v, o);
+  if (s != KB_OK) return s;
+  if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
+  if (L < 1 || start < 0 || kv_cap < 1) return KB_ERR_INVALID_ARG;
+  if (static_cast<long long>(start) + L > kv_cap) return KB_ERR_INVALID_ARG;
+  if (kv_cap > kMaxRows) return KB_ERR_UNSUPPORTED;
+  if (q_tiles_per_cta != 1 && q_tiles_per_cta != 2) return KB_ERR_INVALID_ARG;
+  const int first_tile = start / kb::kTileRows;
+  const int last_tile = (start + L - 1) / kb::kTileRows;
+  const long long grid = static_cast<long long>(last_tile - first_tile + 1) * B * (Hq / q_tiles_per_cta);
+  if (grid > 0x7FFFFFFFLL) return KB_ERR_UNSUPPORTED;
+
+  DeviceState* dst = nullptr;
+  if ((s = get_device_state(&dst)) != KB_OK) return s;
+  for (const void* p : {q, k, v, static_cast<const void*>(o)})
+    if ((s = check_device_pointer(p)) != KB_OK) return s;
+
+  CUtensorMap tq, tk, tv;
+  const uint64_t row_bytes = kb::kHeadDim * 2u;
+  if ((s = encode_rows_map(&tq, q, static_cast<uint64_t>(L), static_cast<uint64_t>(B) * Hq,
+                           static_cast<uint64_t>(L) * row_bytes)) != KB_OK)
+    return s;
+  const uint64_t kv_len = static_cast<uint64_t>(start) + L;
+  if ((s = encode_rows_map(&tk, k, kv_len, static_cast<uint64_t>(B) * Hkv,
+                           static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
+    return s;
+  if ((s = encode_rows_map(&tv, v, kv_len, static_cast<uint64_t>(B) * Hkv,
+                           static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
+    return s;
+
+  kb::PrefillArgs a{};
+  a.o = o;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.L = L;
+  a.start = start;
+  a.first_tile = first_tile;
+  a.n_tiles = last_tile - first_tile + 1;
+  a.err = dst->err;
+  if (kb::launch_prefill(q_tiles_per_cta, tq, tk, tv, a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KB_ERR_CUDA;
+  return KB_OK;
+}
+
+constexpr int kDefaultQTilesPerCta = 2;
+
+}  // namespace
+
+extern "C" {
+
+kb_status kb_attn_chunk(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int L,
+                        int start, int kv_cap, void* stream) {
+  return chunk_impl(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, kDefaultQTilesPerCta, stream);
+}
+
+kb_status kb_attn_chunk_cta_shape(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                                  int L, int start, int kv_cap, int q_tiles_per_cta, void* stream) {
+  return chunk_impl(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, q_tiles_per_cta, stream);
+}
+
+kb_status kb_attn_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int S,
+                          void* stream) {
+  if (S < 1) return KB_ERR_INVALID_ARG;
+  return chunk_impl(q, k, v, o, B, Hq, Hkv, S, 0, S, kDefaultQTilesPerCta, stream);
+}
+
+kb_status kb_attn_decode(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int ctx_len,
+                         int kv_cap, void* stream) {
+  kb_status s = check_ptrs(q, k, v, o);
+  if (s != KB_OK) return s;
+  if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
+  if (ctx_len < 1 || kv_cap < 1 || ctx_len > kv_cap) return KB_ERR_INVALID_ARG;
+  if (kv_cap > kMaxRows) return KB_ERR_UNSUPPORTED;
+
+  DeviceState* dst = nullptr;
+  if ((s = get_device_state(&dst)) != KB_OK) return s;
+  for (const void* p : {q, k, v, static_cast<const void*>(o)})
+    if ((s = check_device_pointer(p)) != KB_OK) return s;
+
+  CUtensorMap tk, tv;
+  const uint64_t row_bytes = kb::kHeadDim * 2u;
+  if ((s = encode_rows_map(&tk, k, static_cast<uint64_t>(ctx_len), static_cast<uint64_t>(B) * Hkv,
+                           static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
+    return s;
+  if ((s = encode_rows_map(&tv, v, static_cast<uint64_t>(ctx_len), static_cast<uint64_t>(B) * Hkv,
+                           static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
+    return s;
+  kb::DecodeArgs a{};
+  a.q = q;
+  a.o = o;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.ctx = ctx_len;
+  a.err = dst->err;
+  if (kb::launch_decode(tk, tv, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KB_ERR_CUDA;
+  return KB_OK;
+}
+
+kb_status kb_attn_check_device_status(void* stream) {
+  DeviceState* dst = nullptr;
+  kb_status s = get_device_state(&dst);
+  if (s != KB_OK) return s;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KB_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, dst->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return KB_ERR_CUDA;
+  if (word != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(dst->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return KB_ERR_CUDA;
+    return KB_ERR_TIMEOUT;
+  }
+  return KB_OK;
+}
+
+kb_status kb_attn_debug_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return KB_ERR_INVALID_ARG;
+  DeviceState* dst = nullptr;
+  kb_status s = get_device_state(&dst);
+  if (s != KB_OK) return s;
+  if (kb::launch_wait_probe(dst->err, static_cast<unsigned long long>(limit_us) * 1000ull,
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KB_ERR_CUDA;
+  return KB_OK;
+}
+
+const char* kb_status_string(kb_status s) {
+  switch (s) {
+    case KB_OK: return "ok";
+    case KB_ERR_INVALID_ARG: return "invalid argument";
+    case KB_ERR_UNSUPPORTED: return "shape outside the numerical contract";
+    case KB_ERR_CUDA: return "CUDA call failed";
+    case KB_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+int kb_contract_version(void) { return kb::kContractVersion; }
+
+}  // extern "C"

@@ -1,0 +1,166 @@
+"""ctypes binding of libkb_attn.so (C ABI in include/kb_attn.h).
+
+Argument marshalling only: every step of the attention runs in the library's
+CUDA kernels.  The functions named like the C entry points take raw device
+pointers; ``prefill`` / ``chunk`` / ``decode`` accept torch CUDA tensors
+(PyTorch is used here only for device memory and streams).
+
+Importing this module loads the library and raises ``ImportError`` when it
+has not been built: there is no fallback implementation.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkb_attn.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with bitwise_aligned_causal_gb300.build.build()")
+_lib = ctypes.CDLL(LIB_PATH)
+
+KB_OK = 0
+KB_ERR_INVALID_ARG = 1
+KB_ERR_UNSUPPORTED = 2
+KB_ERR_CUDA = 3
+KB_ERR_TIMEOUT = 4
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "kb_attn_prefill": [_P, _P, _P, _P, _I, _I, _I, _I, _P],
+    "kb_attn_chunk": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
+    "kb_attn_decode": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
+    "kb_attn_check_device_status": [_P],
+    "kb_attn_debug_wait_timeout": [_I, _P],
+    "kb_attn_chunk_cta_shape": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P],
+    "kb_status_string": [_I],
+    "kb_contract_version": [],
+}
+for _name, _args in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_char_p if _name == "kb_status_string" else ctypes.c_int
+
+EXPORTED = tuple(_SIGS)
+
+
+class KBError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {kb_status_string(status)} (status {status})")
+
+
+def kb_status_string(status: int) -> str:
+    return _lib.kb_status_string(int(status)).decode()
+
+
+def kb_contract_version() -> int:
+    return int(_lib.kb_contract_version())
+
+
+# ---------------------------------------------------------------- raw C entry points
+
+def kb_attn_prefill(q, k, v, o, B, Hq, Hkv, S, stream=None) -> int:
+    return _lib.kb_attn_prefill(q, k, v, o, B, Hq, Hkv, S, stream)
+
+
+def kb_attn_chunk(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, stream=None) -> int:
+    return _lib.kb_attn_chunk(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, stream)
+
+
+def kb_attn_decode(q, k, v, o, B, Hq, Hkv, ctx_len, kv_cap, stream=None) -> int:
+    return _lib.kb_attn_decode(q, k, v, o, B, Hq, Hkv, ctx_len, kv_cap, stream)
+
+
+def kb_attn_chunk_cta_shape(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, q_tiles_per_cta, stream=None) -> int:
+    return _lib.kb_attn_chunk_cta_shape(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, q_tiles_per_cta, stream)
+
+
+def kb_attn_check_device_status(stream=None) -> int:
+    return _lib.kb_attn_check_device_status(stream)
+
+
+def kb_attn_debug_wait_timeout(limit_us, stream=None) -> int:
+    return _lib.kb_attn_debug_wait_timeout(limit_us, stream)
+
+
+# ------------------------------------------------------------------ torch marshalling
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(t, name, ndim):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions [batch, heads, seq, head_dim]")
+
+
+def _raise(status, where):
+    if status != KB_OK:
+        raise KBError(status, where)
+
+
+def prefill(q, k, v, out=None, stream=None):
+    """Causal prefill: q [B,Hq,S,128], k/v [B,Hkv,S,128] -> o shaped like q."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, 4)
+    B, Hq, S, _ = q.shape
+    Hkv = k.shape[1]
+    o = _torch().empty_like(q) if out is None else out
+    _check(o, "out", 4)
+    _raise(kb_attn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, S, _stream(stream)),
+           "kb_attn_prefill")
+    return o
+
+
+def chunk(q, k, v, start, out=None, stream=None, q_tiles_per_cta=None):
+    """Chunked forward: q [B,Hq,L,128] at positions start.., k/v caches [B,Hkv,cap,128]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, 4)
+    B, Hq, L, _ = q.shape
+    Hkv, cap = k.shape[1], k.shape[2]
+    o = _torch().empty_like(q) if out is None else out
+    _check(o, "out", 4)
+    if q_tiles_per_cta is None:
+        st = kb_attn_chunk(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, L, int(start), cap,
+                           _stream(stream))
+    else:
+        st = kb_attn_chunk_cta_shape(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, L,
+                                     int(start), cap, int(q_tiles_per_cta), _stream(stream))
+    _raise(st, "kb_attn_chunk")
+    return o
+
+
+def decode(q, k, v, ctx_len, out=None, stream=None):
+    """One-token decode: q [B,Hq,1,128] at position ctx_len-1, k/v caches [B,Hkv,cap,128]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, 4)
+    B, Hq = q.shape[0], q.shape[1]
+    Hkv, cap = k.shape[1], k.shape[2]
+    o = _torch().empty_like(q) if out is None else out
+    _check(o, "out", 4)
+    _raise(kb_attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, int(ctx_len), cap,
+                          _stream(stream)), "kb_attn_decode")
+    return o
+
+
+def check_device_status(stream=None):
+    _raise(kb_attn_check_device_status(_stream(stream)), "kb_attn_check_device_status")

@@ -1,0 +1,114 @@
+/*
+ * kb_attn.h -- C ABI of libkb_attn.so: bitwise-aligned causal grouped-query
+ * attention forward for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (KernelBraid README, sections "Features" and "Usage / Use a
+ * selected kernel"): BF16 causal attention over contiguous
+ * [batch, heads, sequence, head_dim] tensors, 32 query heads sharing 8 KV
+ * heads (query head h reads KV head h / 4), head_dim 128, scale 1/sqrt(128).
+ * For a query row at absolute position p the output is
+ *     o = sum_{j<=p} softmax_j(q . k_j / sqrt(128)) v_j.
+ *
+ * The three entry points follow one numerical contract (README "Method":
+ * the contract connects full-sequence prefill, partitioned forward execution
+ * and one-token decode; "Advantages": prefill and incremental decode give
+ * bitwise-identical outputs).  A row at position p computed by
+ * kb_attn_prefill, by kb_attn_chunk (any split of the sequence) and by
+ * kb_attn_decode (ctx_len = p + 1) has the same bf16 bits.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *    bf16, contiguous, 16-byte aligned, owned by the caller.  The library
+ *    never allocates, frees or keeps them.
+ *  - Hq must equal 4 * Hkv (the GQA group size of the contract); head_dim is
+ *    fixed at 128.  Other shapes return KB_ERR_UNSUPPORTED.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and do not synchronise the host.  Argument errors are
+ *    reported before anything is enqueued.  A device-side wait that gave up
+ *    (never expected) is reported by kb_attn_check_device_status.
+ *  - Rows of the KV cache beyond the visible context are never used, so they
+ *    may hold anything (including NaN bit patterns).
+ */
+#ifndef KB_ATTN_H
+#define KB_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kb_status {
+    KB_OK = 0,
+    KB_ERR_INVALID_ARG = 1,   /* null or misaligned pointer, non-positive size, not device memory */
+    KB_ERR_UNSUPPORTED = 2,   /* shape outside the contract (Hq != 4*Hkv, sizes too large) */
+    KB_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed */
+    KB_ERR_TIMEOUT = 4        /* a bounded device-side wait gave up (see kb_attn_check_device_status) */
+} kb_status;
+
+/*
+ * Full-sequence causal prefill (README "Usage": unified_prefill(q, k, v, H_Q, H_KV)).
+ *   q, o : [B, Hq, S, 128]   query rows are positions 0..S-1; o has q's shape
+ *   k, v : [B, Hkv, S, 128]
+ * Identical to kb_attn_chunk(q, k, v, o, B, Hq, Hkv, S, 0, S, stream).
+ */
+kb_status kb_attn_prefill(const void* q, const void* k, const void* v, void* o,
+                          int B, int Hq, int Hkv, int S, void* stream);
+
+/*
+ * Partitioned (chunked) forward against a KV cache (README "Method":
+ * partitioned forward execution; "Usage": prompt/answer splits).
+ *   q, o : [B, Hq, L, 128]       query row i is absolute position start + i
+ *   k, v : [B, Hkv, kv_cap, 128] rows 0..start+L-1 must already hold the keys
+ *                                and values of every position up to the chunk's
+ *                                last row (the caller appends the chunk's own
+ *                                K/V before the call)
+ * Requires L >= 1, start >= 0, start + L <= kv_cap.
+ */
+kb_status kb_attn_chunk(const void* q, const void* k, const void* v, void* o,
+                        int B, int Hq, int Hkv, int L, int start, int kv_cap, void* stream);
+
+/*
+ * One-token decode (README "Usage": unified_decode(q[:, :, -1:], k, v, H_Q, H_KV)).
+ *   q, o : [B, Hq, 1, 128]       the query sits at position ctx_len - 1
+ *   k, v : [B, Hkv, kv_cap, 128] rows 0..ctx_len-1 are the visible context
+ * Requires 1 <= ctx_len <= kv_cap.
+ */
+kb_status kb_attn_decode(const void* q, const void* k, const void* v, void* o,
+                         int B, int Hq, int Hkv, int ctx_len, int kv_cap, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device-side
+ * error word on the current device.  Returns KB_ERR_TIMEOUT if any kernel
+ * since the last check gave up on a bounded wait (its output is then
+ * undefined), KB_ERR_CUDA if the synchronisation failed, else KB_OK.
+ */
+kb_status kb_attn_check_device_status(void* stream);
+
+/*
+ * Test hook for the failure path: enqueues a one-CTA kernel that waits on a
+ * barrier nothing will signal, giving up after `limit_us` microseconds
+ * (1..1000000).  A following kb_attn_check_device_status returns
+ * KB_ERR_TIMEOUT.  Faults and hangs nothing.
+ */
+kb_status kb_attn_debug_wait_timeout(int limit_us, void* stream);
+
+/*
+ * Prefill/chunk with an explicit CTA shape, for tests of the contract: the
+ * kernel runs q_tiles_per_cta (1 or 2) query tiles per CTA.  Both shapes give
+ * the same bits as kb_attn_chunk.
+ */
+kb_status kb_attn_chunk_cta_shape(const void* q, const void* k, const void* v, void* o,
+                                  int B, int Hq, int Hkv, int L, int start, int kv_cap,
+                                  int q_tiles_per_cta, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* kb_status_string(kb_status s);
+
+/* Version of the numerical contract; outputs are bit-identical across builds
+ * with the same contract version on the same GPU architecture. */
+int kb_contract_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KB_ATTN_H */

@@ -1,0 +1,79 @@
+"""The C ABI: the library loads on a machine without a GPU, exports every
+symbol include/kb_attn.h declares, and rejects bad arguments before it makes
+any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kb_attn.h")
+
+
+@pytest.fixture(scope="module")
+def kb():
+    from bitwise_aligned_causal_gb300 import build
+
+    build.build()
+    from bitwise_aligned_causal_gb300 import kb_attn
+
+    return kb_attn
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kb_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("kb_attn_prefill", "kb_attn_chunk", "kb_attn_decode", "kb_attn_check_device_status",
+              "kb_status_string", "kb_contract_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(kb):
+    lib = ctypes.CDLL(kb.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in kb_attn.h but not exported"
+    assert set(declared_functions()) == set(kb.EXPORTED)
+
+
+def test_status_strings_and_version(kb):
+    assert kb.kb_status_string(0) == "ok"
+    assert "timed out" in kb.kb_status_string(4)
+    assert kb.kb_status_string(99) == "unknown status"
+    assert kb.kb_contract_version() == 1
+
+
+FAKE = 0x1000_0000     # aligned, non-null; never dereferenced by the host checks below
+
+
+def test_null_and_misaligned_pointers_rejected(kb):
+    assert kb.kb_attn_prefill(None, FAKE, FAKE, FAKE, 1, 32, 8, 16) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_prefill(FAKE + 2, FAKE, FAKE, FAKE, 1, 32, 8, 16) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_decode(FAKE, FAKE, FAKE, None, 1, 32, 8, 1, 1) == kb.KB_ERR_INVALID_ARG
+
+
+def test_shapes_outside_the_contract_rejected(kb):
+    assert kb.kb_attn_prefill(FAKE, FAKE, FAKE, FAKE, 1, 32, 4, 16) == kb.KB_ERR_UNSUPPORTED
+    assert kb.kb_attn_prefill(FAKE, FAKE, FAKE, FAKE, 1, 30, 8, 16) == kb.KB_ERR_UNSUPPORTED
+    assert kb.kb_attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 8, 8, 4, 4) == kb.KB_ERR_UNSUPPORTED
+    assert kb.kb_attn_chunk(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 16, 0, 1 << 23) == kb.KB_ERR_UNSUPPORTED
+
+
+def test_bad_sizes_rejected(kb):
+    for args in [(0, 32, 8, 16), (1, 32, 8, 0), (-1, 32, 8, 4), (1, 0, 0, 4)]:
+        assert kb.kb_attn_prefill(FAKE, FAKE, FAKE, FAKE, *args) in (kb.KB_ERR_INVALID_ARG, kb.KB_ERR_UNSUPPORTED)
+    # chunk must fit in the cache
+    assert kb.kb_attn_chunk(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 10, 100, 109) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_chunk(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 0, 0, 10) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_chunk(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 4, -1, 10) == kb.KB_ERR_INVALID_ARG
+    # decode context within the cache
+    assert kb.kb_attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 11, 10) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 0, 10) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 4, 0, 10, 3) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_debug_wait_timeout(0) == kb.KB_ERR_INVALID_ARG
