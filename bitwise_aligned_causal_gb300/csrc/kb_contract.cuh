@@ -5,7 +5,7 @@
 // one-token decode, so that the three produce bitwise-identical output rows
 // for the same inputs and context ("Advantages"; the "Usage" example compares
 // the raw bf16 bits).  The pages do not print the contract's contents, so it
-// is fixed here, version 1:
+// is fixed here, version 2:
 //
 //  C1 One KV tile of 128 keys, anchored at key 0, visited in ascending order
 //     0..floor(p/128) for a row at absolute position p.  Prefill/chunk query
@@ -15,7 +15,8 @@
 //     M=128 N=128 K=16.  S = Q K^T and O += P V each issue eight of them in
 //     ascending K order; S is A/B from shared memory, P V reads P from TMEM.
 //  C3 One thread owns one row of S and O (TMEM lane = row).  All row math is
-//     the functions below; data-dependent choices are per row only.
+//     the functions below; data-dependent choices (when the reference max
+//     moves, which keys are masked) are per row only.
 //  C4 One normalisation: o = bf16_rn(O * rcp_rn(l)).
 //  C5 No split of the KV range (a split would be a fixed, length-determined
 //     partition folded identically by every entry point).
@@ -34,7 +35,7 @@ constexpr int kHeadDim = 128;      // D
 constexpr int kTileKeys = 128;     // keys per KV tile (C1)
 constexpr int kTileRows = 128;     // query rows per tile = MMA M (C2)
 constexpr int kGroup = 4;          // query heads per KV head (32 / 8)
-constexpr int kContractVersion = 1;
+constexpr int kContractVersion = 2;
 
 // c = log2(e) / sqrt(128) = 0.1275174308245986852... rounded to the nearest
 // fp32, bit pattern 0x3E0293EE.  The softmax weight of score s against the
@@ -83,70 +84,108 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
 
 // Per-row running state of the online softmax.
 struct RowState {
-  float m;  // running max of the raw scores q.k (unscaled)
-  float l;  // running sum of the fp32 weights
+  float m;   // reference max of the raw scores q.k (unscaled); -inf before the first tile
+  float mc;  // m * c, rounded to fp32
+  float l;   // running sum of the fp32 weights
 };
 
-__device__ __forceinline__ RowState row_state_init() { return RowState{-INFINITY, 0.0f}; }
+__device__ __forceinline__ RowState row_state_init() { return RowState{-INFINITY, -INFINITY, 0.0f}; }
+
+// The reference max moves only when a tile's max exceeds it by more than
+// this many raw score units (64 * c = 8.16 in log2 units), so weights stay
+// below 2^8.2 and the O rescale is rare.  The decision is per row.
+constexpr float kRescaleThresholdRaw = 64.0f;
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 // One KV tile of the online softmax for one row (C3).
 //
 //  s[k]     raw scores q.k of keys 128j+k (fp32 bit patterns from TMEM)
-//  n_valid  number of visible keys in this tile (keys >= n_valid are masked);
-//           128 except on the row's last tile
+//  kMasked  true only on the row's last tile; then keys k >= n_valid are
+//           masked to -inf (a select, so an all-visible tile gives the same
+//           bits either way)
 //  p        out: the weights rounded to bf16, packed two per word, key 2i in
 //           the low half of p[i]
 //  returns  alpha, the factor the row's O accumulator must be scaled by
-//           before this tile's P V is added (exactly 1.0 when the max did not
-//           change, exactly 0.0 on the first tile)
+//           before this tile's P V is added (exactly 1.0 when the reference
+//           max did not move, exactly 0.0 on the first tile)
 //
-//  m'    = max(m, max_k s[k])                          (exact)
-//  mc    = m' * c                                      (c = log2(e)/sqrt(128))
-//  alpha = 1 if m' == m else 2^(fma(m, c, -mc))
-//  w[k]  = 2^(fma(s[k], c, -mc)),  masked keys -> +0
-//  l'    = fma(l, alpha, sum_k w[k]) with the sum taken as eight strided
-//          partial sums (k mod 8, ascending k) combined as a balanced tree
+//  t     = max_k s[k]                                          (exact)
+//  if t - m > 64 (always on the first tile, where m = -inf):
+//        m' = t, mc' = m' * c, alpha = 2^(fma(m, c, -mc'))
+//  else  m' = m, mc' = mc, alpha = 1
+//  w[k]  = 2^(fma(s[k], c, -mc'))   (masked keys -> +0)
+//  l'    = fma(l, alpha, sum_k w[k]), the sum taken as eight strided partial
+//          sums (k mod 8, ascending k) combined as ((0+1)+(2+3))+((4+5)+(6+7))
+// with c = log2(e)/sqrt(128) in fp32 and 2^x the hardware ex2.approx.ftz.
+template <bool kMasked>
 __device__ __forceinline__ float row_softmax_tile(const uint32_t (&s)[128], int n_valid, RowState& st,
                                                   uint32_t (&p)[64]) {
   const float c = score_scale_log2();
   float x[128];
 #pragma unroll
-  for (int k = 0; k < 128; ++k) x[k] = (k < n_valid) ? __uint_as_float(s[k]) : -INFINITY;
-
-  float mx[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) mx[i] = x[i];
-#pragma unroll
-  for (int k = 8; k < 128; ++k) mx[k & 7] = fmaxf(mx[k & 7], x[k]);
-  const float tile_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-  const float m_new = fmaxf(st.m, tile_max);
-  const float mc = __fmul_rn(m_new, c);
-  const float neg_mc = -mc;
-  const float alpha = (m_new == st.m) ? 1.0f : ex2_approx(__fmaf_rn(st.m, c, neg_mc));
-
-  float acc[8];
-#pragma unroll
   for (int k = 0; k < 128; ++k) {
-    const float w = ex2_approx(__fmaf_rn(x[k], c, neg_mc));
-    x[k] = w;
-    if (k < 8) acc[k] = w;
-    else acc[k & 7] = __fadd_rn(acc[k & 7], w);
+    x[k] = __uint_as_float(s[k]);
+    if (kMasked) x[k] = (k < n_valid) ? x[k] : -INFINITY;
   }
-  const float tile_sum = __fadd_rn(__fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3])),
-                                   __fadd_rn(__fadd_rn(acc[4], acc[5]), __fadd_rn(acc[6], acc[7])));
+
+  // exact row max (max is order-free): 16 lanes of three-input maxima
+  float mx[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    mx[i] = max3(x[i], x[i + 16], x[i + 32]);
+    mx[i] = max3(mx[i], x[i + 48], x[i + 64]);
+    mx[i] = max3(mx[i], x[i + 80], x[i + 96]);
+    mx[i] = fmaxf(mx[i], x[i + 112]);
+  }
+#pragma unroll
+  for (int i = 0; i < 5; ++i) mx[i] = max3(mx[i], mx[i + 5], mx[i + 10]);
+  const float tile_max = max3(max3(mx[0], mx[1], mx[2]), mx[3], fmaxf(mx[4], mx[15]));
+
+  float alpha = 1.0f;
+  if (__fsub_rn(tile_max, st.m) > kRescaleThresholdRaw) {
+    const float mc_new = __fmul_rn(tile_max, c);
+    alpha = ex2_approx(__fmaf_rn(st.m, c, -mc_new));
+    st.m = tile_max;
+    st.mc = mc_new;
+  }
+  const float2 c2 = make_float2(c, c);
+  const float2 nmc2 = make_float2(-st.mc, -st.mc);
+
+  float2 acc[4];
+#pragma unroll
+  for (int k = 0; k < 128; k += 2) {
+    const float2 arg = __ffma2_rn(make_float2(x[k], x[k + 1]), c2, nmc2);
+    const float w0 = ex2_approx(arg.x);
+    const float w1 = ex2_approx(arg.y);
+    x[k] = w0;
+    x[k + 1] = w1;
+    const int a = (k & 7) >> 1;
+    if (k < 8) acc[a] = make_float2(w0, w1);
+    else acc[a] = __fadd2_rn(acc[a], make_float2(w0, w1));
+  }
+  const float tile_sum = __fadd_rn(__fadd_rn(__fadd_rn(acc[0].x, acc[0].y), __fadd_rn(acc[1].x, acc[1].y)),
+                                   __fadd_rn(__fadd_rn(acc[2].x, acc[2].y), __fadd_rn(acc[3].x, acc[3].y)));
 #pragma unroll
   for (int i = 0; i < 64; ++i) p[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
 
   st.l = __fmaf_rn(st.l, alpha, tile_sum);
-  st.m = m_new;
   return alpha;
 }
 
 // Scale 32 accumulator columns by alpha (bit-neutral when alpha == 1).
 __device__ __forceinline__ void rescale32(uint32_t (&o)[32], float alpha) {
+  const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__fmul_rn(__uint_as_float(o[i]), alpha));
+  for (int i = 0; i < 32; i += 2) {
+    const float2 r = __fmul2_rn(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+    o[i] = __float_as_uint(r.x);
+    o[i + 1] = __float_as_uint(r.y);
+  }
 }
 
 // C4: final normalisation of 32 accumulator columns into 16 bf16 pairs.

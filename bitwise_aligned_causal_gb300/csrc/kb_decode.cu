@@ -185,9 +185,9 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       const uint32_t s_tmem = tmem_base + (j & 1) * 128u;
       uint32_t s[128];
       tmem_ld128_wait(s_tmem, s);
-      const int n_valid = (j == n_kv - 1) ? (ctx - j * kTileKeys) : kTileKeys;
       uint32_t p[64];
-      const float alpha = row_softmax_tile(s, n_valid, st, p);
+      const float alpha = (j == n_kv - 1) ? row_softmax_tile<true>(s, ctx - j * kTileKeys, st, p)
+                                          : row_softmax_tile<false>(s, kTileKeys, st, p);
       if (j > 0) {
         ok = mbar_wait(bar(Cfg::kBarOFull), (j - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
         ok = __all_sync(0xffffffffu, ok);

@@ -26,17 +26,26 @@ struct DeviceState {
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+// Record a failed CUDA call for kb_attn_last_cuda_error and map it to a status.
+kb_status cuda_fail(cudaError_t e) {
+  t_last_cuda_error = e;
+  (void)cudaGetLastError();
+  return KB_ERR_CUDA;
+}
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 kb_status get_device_state(DeviceState** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return KB_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return KB_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& st = g_dev[dev];
   if (!st.ready) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_kb_error_word) != cudaSuccess) return KB_ERR_CUDA;
+    if ((e = cudaGetSymbolAddress(&p, g_kb_error_word)) != cudaSuccess) return cuda_fail(e);
     st.err = static_cast<uint32_t*>(p);
     st.ready = true;
   }
@@ -138,12 +147,12 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   a.first_tile = first_tile;
   a.n_tiles = last_tile - first_tile + 1;
   a.err = dst->err;
-  if (kb::launch_prefill(q_tiles_per_cta, tq, tk, tv, a, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return KB_ERR_CUDA;
+  const cudaError_t e = kb::launch_prefill(q_tiles_per_cta, tq, tk, tv, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
   return KB_OK;
 }
 
-constexpr int kDefaultQTilesPerCta = 2;
+constexpr int kDefaultQTilesPerCta = 1;
 
 }  // namespace
 
@@ -194,7 +203,8 @@ kb_status kb_attn_decode(const void* q, const void* k, const void* v, void* o, i
   a.Hkv = Hkv;
   a.ctx = ctx_len;
   a.err = dst->err;
-  if (kb::launch_decode(tk, tv, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KB_ERR_CUDA;
+  const cudaError_t e = kb::launch_decode(tk, tv, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
   return KB_OK;
 }
 
@@ -202,12 +212,13 @@ kb_status kb_attn_check_device_status(void* stream) {
   DeviceState* dst = nullptr;
   kb_status s = get_device_state(&dst);
   if (s != KB_OK) return s;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KB_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
   uint32_t word = 0;
-  if (cudaMemcpy(&word, dst->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return KB_ERR_CUDA;
+  if ((e = cudaMemcpy(&word, dst->err, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
   if (word != 0) {
     const uint32_t zero = 0;
-    if (cudaMemcpy(dst->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return KB_ERR_CUDA;
+    if ((e = cudaMemcpy(dst->err, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess) return cuda_fail(e);
     return KB_ERR_TIMEOUT;
   }
   return KB_OK;
@@ -218,9 +229,9 @@ kb_status kb_attn_debug_wait_timeout(int limit_us, void* stream) {
   DeviceState* dst = nullptr;
   kb_status s = get_device_state(&dst);
   if (s != KB_OK) return s;
-  if (kb::launch_wait_probe(dst->err, static_cast<unsigned long long>(limit_us) * 1000ull,
-                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return KB_ERR_CUDA;
+  const cudaError_t e = kb::launch_wait_probe(dst->err, static_cast<unsigned long long>(limit_us) * 1000ull,
+                                              static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
   return KB_OK;
 }
 
@@ -236,5 +247,9 @@ const char* kb_status_string(kb_status s) {
 }
 
 int kb_contract_version(void) { return kb::kContractVersion; }
+
+int kb_attn_last_cuda_error(void) { return static_cast<int>(t_last_cuda_error); }
+
+const char* kb_attn_last_cuda_error_string(void) { return cudaGetErrorString(t_last_cuda_error); }
 
 }  // extern "C"

@@ -25,6 +25,9 @@ struct PrefillCfg {
   static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
   static constexpr int kStages = (NQ == 1) ? 1 : 2;
   static constexpr uint32_t kTmemCols = (NQ == 1) ? 256u : 512u;
+  // Registers are split evenly over the SM's four sub-partitions, so a CTA of
+  // 10 warps (3 on some sub-partition) gets at most 168 per thread, as do two
+  // resident CTAs of 6 warps.
   static constexpr int kMinBlocks = (NQ == 1) ? 2 : 1;
 
   static constexpr uint32_t kQOff = 0;
@@ -152,24 +155,26 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
     }
   } else if (warp == Cfg::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
+    // Issue order (NQ = 2): S0(0) S1(0) | O0+=P0V(0) S0(1) O1+=P1V(0) S1(1) |
+    // O0+=P0V(1) S0(2) ...  so each query tile's softmax overlaps the other
+    // tile's two products.  P of a query tile lives in the first 64 columns
+    // of its S buffer; the next S of that tile is issued after its P V, and
+    // tcgen05.mma instructions from one thread execute in issue order.
     if (lane == 0 && !skip) {
       bool ok = mbar_wait(bar(Cfg::kBarQFull), 0, abort_flag, args.err, kDevTimeoutTma);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int slot = j % Cfg::kStages;
-        const uint32_t use = j / Cfg::kStages;
-        ok = mbar_wait(bar(Cfg::kBarKFull + slot), use & 1, abort_flag, args.err, kDevTimeoutTma);
-        for (int qi = 0; qi < NQ && ok; ++qi) {
-          // S/P of this query tile is free once P V of the previous tile is done
-          if (j > 0) ok = mbar_wait(bar(Cfg::kBarOFull + qi), (j - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
-          if (!ok) break;
-          tc_fence_after();
-          issue_qk(tmem_base + qi * 256u, sbase + Cfg::kQOff + qi * kTileBytes, 1024u, kSlabBytes,
-                   sbase + Cfg::kKOff + slot * kTileBytes);
+      if (ok) ok = mbar_wait(bar(Cfg::kBarKFull), 0, abort_flag, args.err, kDevTimeoutTma);
+      if (ok) {
+        tc_fence_after();
+        for (int qi = 0; qi < NQ; ++qi) {
+          issue_qk(tmem_base + qi * 256u, sbase + Cfg::kQOff + qi * kTileBytes, 1024u, kSlabBytes, sbase + Cfg::kKOff);
           tc_commit(bar(Cfg::kBarSFull + qi));
         }
-        if (!ok) break;
-        tc_commit(bar(Cfg::kBarKEmpty + slot));
-        ok = mbar_wait(bar(Cfg::kBarVFull + slot), use & 1, abort_flag, args.err, kDevTimeoutTma);
+        tc_commit(bar(Cfg::kBarKEmpty));
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int slot = j % Cfg::kStages;
+        const int nslot = (j + 1) % Cfg::kStages;
+        ok = mbar_wait(bar(Cfg::kBarVFull + slot), (j / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
         for (int qi = 0; qi < NQ && ok; ++qi) {
           ok = mbar_wait(bar(Cfg::kBarPFull + qi), j & 1, abort_flag, args.err, kDevTimeoutSoftmax);
           if (!ok) break;
@@ -177,9 +182,20 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
           issue_pv(tmem_base + qi * 256u + 128u, tmem_base + qi * 256u, sbase + Cfg::kVOff + slot * kTileBytes,
                    j == 0);
           tc_commit(bar(Cfg::kBarOFull + qi));
+          if (qi == NQ - 1) tc_commit(bar(Cfg::kBarVEmpty + slot));
+          if (j + 1 < n_kv) {
+            if (qi == 0) {
+              ok = mbar_wait(bar(Cfg::kBarKFull + nslot), ((j + 1) / Cfg::kStages) & 1, abort_flag, args.err,
+                             kDevTimeoutTma);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_qk(tmem_base + qi * 256u, sbase + Cfg::kQOff + qi * kTileBytes, 1024u, kSlabBytes,
+                     sbase + Cfg::kKOff + nslot * kTileBytes);
+            tc_commit(bar(Cfg::kBarSFull + qi));
+            if (qi == NQ - 1) tc_commit(bar(Cfg::kBarKEmpty + nslot));
+          }
         }
-        if (!ok) break;
-        tc_commit(bar(Cfg::kBarVEmpty + slot));
       }
       if (!ok) {
         tc_commit(bar(Cfg::kBarDrain));   // arrives once every MMA issued so far has finished
@@ -202,9 +218,9 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
       tc_fence_after();
       uint32_t s[128];
       tmem_ld128_wait(s_tmem, s);
-      const int n_valid = (j == n_kv - 1) ? (r + 1) : kTileKeys;   // causal mask on the diagonal tile
       uint32_t p[64];
-      const float alpha = row_softmax_tile(s, n_valid, st, p);
+      const float alpha = (j == n_kv - 1) ? row_softmax_tile<true>(s, r + 1, st, p)   // diagonal tile: causal mask
+                                          : row_softmax_tile<false>(s, kTileKeys, st, p);
       if (j > 0) {
         ok = mbar_wait(bar(Cfg::kBarOFull + qi), (j - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
         ok = __all_sync(0xffffffffu, ok);

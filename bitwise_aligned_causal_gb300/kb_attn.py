@@ -38,11 +38,13 @@ _SIGS = {
     "kb_attn_chunk_cta_shape": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P],
     "kb_status_string": [_I],
     "kb_contract_version": [],
+    "kb_attn_last_cuda_error": [],
+    "kb_attn_last_cuda_error_string": [],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
-    _f.restype = ctypes.c_char_p if _name == "kb_status_string" else ctypes.c_int
+    _f.restype = ctypes.c_char_p if _name.endswith("string") else ctypes.c_int
 
 EXPORTED = tuple(_SIGS)
 
@@ -50,7 +52,10 @@ EXPORTED = tuple(_SIGS)
 class KBError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {kb_status_string(status)} (status {status})")
+        msg = f"{where}: {kb_status_string(status)} (status {status})"
+        if status == KB_ERR_CUDA:
+            msg += f": {kb_attn_last_cuda_error_string()} (cudaError {kb_attn_last_cuda_error()})"
+        super().__init__(msg)
 
 
 def kb_status_string(status: int) -> str:
@@ -59,6 +64,14 @@ def kb_status_string(status: int) -> str:
 
 def kb_contract_version() -> int:
     return int(_lib.kb_contract_version())
+
+
+def kb_attn_last_cuda_error() -> int:
+    return int(_lib.kb_attn_last_cuda_error())
+
+
+def kb_attn_last_cuda_error_string() -> str:
+    return _lib.kb_attn_last_cuda_error_string().decode()
 
 
 # ---------------------------------------------------------------- raw C entry points

@@ -100,6 +100,11 @@ kb_status kb_attn_chunk_cta_shape(const void* q, const void* k, const void* v, v
                                   int B, int Hq, int Hkv, int L, int start, int kv_cap,
                                   int q_tiles_per_cta, void* stream);
 
+/* The cudaError_t code (as int) and its description for the most recent
+ * KB_ERR_CUDA returned on the calling host thread; 0 / "no error" if none. */
+int kb_attn_last_cuda_error(void);
+const char* kb_attn_last_cuda_error_string(void);
+
 /* Static description of a status code (never NULL). */
 const char* kb_status_string(kb_status s);
 

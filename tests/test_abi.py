@@ -46,7 +46,7 @@ def test_status_strings_and_version(kb):
     assert kb.kb_status_string(0) == "ok"
     assert "timed out" in kb.kb_status_string(4)
     assert kb.kb_status_string(99) == "unknown status"
-    assert kb.kb_contract_version() == 1
+    assert kb.kb_contract_version() == 2
 
 
 FAKE = 0x1000_0000     # aligned, non-null; never dereferenced by the host checks below

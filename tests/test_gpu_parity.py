@@ -124,12 +124,16 @@ def test_cta_shapes_give_identical_bits(kb):
 
 
 def test_repeat_runs_are_identical(kb):
-    x = inputs.make_qkv(1, 1100, seed=41_000)
+    """Eight back-to-back runs give the same bits (no order- or timing-dependent arithmetic)."""
+    import torch
+
+    x = inputs.make_qkv(2, 4100, seed=41_000)
     q, k, v = to_dev(x.q), to_dev(x.k), to_dev(x.v)
-    a = from_dev(kb.prefill(q, k, v))
-    b = from_dev(kb.prefill(q, k, v))
+    outs = [kb.prefill(q, k, v) for _ in range(8)]
     kb.check_device_status()
-    assert np.array_equal(a, b)
+    ref = outs[0].view(torch.int16)
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), ref)
 
 
 @pytest.mark.parametrize("start,L", [(0, 1), (1, 1), (127, 1), (128, 1), (5, 300), (130, 126), (256, 128),
