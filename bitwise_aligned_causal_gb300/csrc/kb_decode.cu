@@ -1,30 +1,40 @@
-// kb_decode.cu -- one-token decode over a contiguous KV cache (KernelBraid
+// kb_decode.cu -- query rows packed by GQA group: one-token decode (KernelBraid
 // README, "Usage": unified_decode over the same KV context, whose output must
 // equal the prefill row bit for bit; "Features": one query token per decode
-// call).
+// call) and chunks of up to 32 query rows against a KV cache (README
+// "Method": partitioned forward execution), on a contiguous or a paged cache.
 //
-// One CTA per (batch, KV head).  The four query heads of the GQA group are
-// packed into rows 0..3 of the M=128 MMA (rows 4..7 are zero and row groups
-// 8..127 alias rows 0..7 through a zero stride-byte-offset descriptor), so
-// decode issues the very same tcgen05.mma shape, k-order and row softmax as
-// prefill and every packed row reproduces the prefill row exactly.  K/V tiles
-// stream through a three-deep TMA ring; S is double-buffered in TMEM so the
-// next Q K^T overlaps the current softmax.
-//   warp 0  softmax (TMEM lanes 0..31; lanes 0..3 are the four heads)
-//   warp 1  TMA producer (one lane)
-//   warp 2  TMEM allocator + MMA issuer (one lane)
+// One CTA per (sub-chunk, batch, KV head).  The four query heads of the GQA
+// group and the sub-chunk's rows are packed into the rows of the M=128 MMA
+// (row m = head i * Lc + query row r), so the CTA issues the very same
+// tcgen05.mma shape, k-order and row softmax as prefill and every packed row
+// reproduces the prefill row exactly, while K and V are read once per KV head.
+// A sub-chunk never crosses a 128-position tile boundary, so all its rows end
+// on the same KV tile.  K/V tiles stream through a three-deep TMA ring; S is
+// double-buffered in TMEM so the next Q K^T overlaps the current softmax.
+//   warps 0..NS-1  softmax (TMEM lanes 32w..32w+31; NS = 1 narrow, 4 wide)
+//   warp  NS       TMA producer (lane 0 issues; the warp zeroes a V tail)
+//   warp  NS+1     TMEM allocator + MMA issuer (one lane)
+// Narrow (at most 8 packed rows): Q is one 8-row swizzle atom per d-slab and
+// the row groups 8..127 of the MMA alias it (stride-byte-offset 0).
 #include "kb_contract.cuh"
 #include "kb_launch.h"
 
 namespace kb {
 
-struct DecodeCfg {
-  static constexpr int kThreads = 96;
+template <bool kWide>
+struct PackedCfg {
+  static constexpr int kSoftmaxWarps = kWide ? 4 : 1;
+  static constexpr int kProdWarp = kSoftmaxWarps;
+  static constexpr int kMmaWarp = kSoftmaxWarps + 1;
+  static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
   static constexpr int kStages = 3;
-  static constexpr uint32_t kTmemCols = 512;   // S0, S1, O (128 columns each)
-  static constexpr uint32_t kQAtom = 1024;     // 8 rows x 128 bytes, one per d-slab
+  static constexpr int kQRows = kWide ? 128 : 8;
+  static constexpr uint32_t kTmemCols = 512;                  // S0, S1, O (128 columns each)
+  static constexpr uint32_t kQSlab = kQRows * 128;            // bytes of one 64-column slab of Q
+  static constexpr uint32_t kQSbo = kWide ? 1024u : 0u;
   static constexpr uint32_t kQOff = 0;
-  static constexpr uint32_t kKOff = 2 * kQAtom;
+  static constexpr uint32_t kKOff = 2 * kQSlab;
   static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
   static constexpr uint32_t kBarOff = kVOff + kStages * kTileBytes;
   static constexpr int kBarKFull = 0;
@@ -34,23 +44,42 @@ struct DecodeCfg {
   static constexpr int kBarSFull = kBarVEmpty + kStages;   // 2 (double-buffered S)
   static constexpr int kBarPFull = kBarSFull + 2;
   static constexpr int kBarOFull = kBarPFull + 1;
-  static constexpr int kBarDrain = kBarOFull + 1;
+  static constexpr int kBarVReady = kBarOFull + 1;         // last V tile with its tail zeroed
+  static constexpr int kBarDrain = kBarVReady + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemUsed = kMiscOff + 16;
   static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;
 };
 
-__device__ __forceinline__ void decode_drain_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void packed_drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity))
     if (global_timer_ns() - t0 > 50000000ull) break;
 }
 
-__global__ void __launch_bounds__(DecodeCfg::kThreads, 1)
+// Row of the K/V tensor map and plane of key tile j of sequence b, KV head g.
+__device__ __forceinline__ void kv_tile_coords(const PackedArgs& a, int b, int g, int j, int& row, int& plane) {
+  if (a.block_table == nullptr) {
+    row = j * kTileKeys;
+    plane = b * a.Hkv + g;
+    return;
+  }
+  const int key = j * kTileKeys;
+  int pg = a.block_table[static_cast<size_t>(b) * a.pages_per_seq + key / a.page_size];
+  if (pg < 0 || pg >= a.num_pages) {
+    atomicCAS(a.err, 0u, static_cast<uint32_t>(kDevBadInput));
+    pg = a.num_pages;          // beyond the map: the TMA unit reads zeros
+  }
+  row = key % a.page_size;
+  plane = pg * a.Hkv + g;
+}
+
+template <bool kWide>
+__global__ void __launch_bounds__(PackedCfg<kWide>::kThreads, 1)
 kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                 const DecodeArgs args) {
-  using Cfg = DecodeCfg;
+                 const PackedArgs args) {
+  using Cfg = PackedCfg<kWide>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
@@ -61,34 +90,59 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x / args.Hkv;
+  const int bh = args.B * args.Hkv;
+  const int sub = blockIdx.x / bh;
+  const int b = (blockIdx.x % bh) / args.Hkv;
   const int g = blockIdx.x % args.Hkv;
-  const int ctx = args.ctx;
-  const int n_kv = (ctx - 1) / kTileKeys + 1;     // C1: KV tiles 0..floor((ctx-1)/128)
 
-  // Q rows 0..3 = heads 4g..4g+3, rows 4..7 = 0, written in the 128-byte
-  // swizzled layout the MMA descriptor expects (16-byte chunk c of row r
-  // sits at chunk c ^ r).
-  {
-    const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(args.q) +
-                                                       (static_cast<size_t>(b) * args.Hq + g * kGroup) * kHeadDim);
-    for (int idx = threadIdx.x; idx < 8 * 16; idx += Cfg::kThreads) {
-      const int row = idx >> 4;
-      const int c = idx & 15;
-      const int slab = c >> 3;
-      const int cc = c & 7;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (row < kGroup) val = __ldg(qsrc + row * (kHeadDim / 8) + c);
-      *reinterpret_cast<uint4*>(smem + Cfg::kQOff + slab * Cfg::kQAtom + row * 128 + ((cc ^ row) << 4)) = val;
+  // Absolute position of query row 0, the sub-chunk's rows [r0, r1) and the
+  // key range of the sequence (keys at or beyond seq_kv are never used).
+  int pos0 = args.start;
+  if (args.ctx_lens != nullptr) {
+    const int ctx = args.ctx_lens[b];
+    if (ctx < args.L || ctx > args.max_ctx) {
+      if (threadIdx.x == 0) atomicCAS(args.err, 0u, static_cast<uint32_t>(kDevBadInput));
+      return;
     }
+    pos0 = ctx - args.L;
+  }
+  const int seq_kv = pos0 + args.L;
+  const int split = min(args.L, (pos0 / kTileKeys + 1) * kTileKeys - pos0);   // rows before the first tile boundary
+  const int r0 = (sub == 0) ? 0 : split;
+  const int r1 = (sub == 0) ? split : args.L;
+  const int Lc = r1 - r0;
+  if (Lc <= 0) return;                                  // the chunk does not reach a second tile
+  const int n_rows = kGroup * Lc;                       // packed rows in use
+  const int n_kv = (pos0 + r1 - 1) / kTileKeys + 1;     // C1: KV tiles 0..floor(last position / 128)
+  const bool zero_tail = (args.block_table != nullptr) || (args.ctx_lens != nullptr);
+  const int tail_from = seq_kv - (n_kv - 1) * kTileKeys;   // first V row of the last tile past the sequence
+
+  // Q: packed row m = head i * Lc + rr holds q[b, 4g+i, r0+rr]; unused rows
+  // are zero.  Written in the 128-byte swizzled layout the MMA descriptor
+  // expects (16-byte chunk c of row m sits at chunk c ^ (m % 8)).
+  for (int idx = threadIdx.x; idx < Cfg::kQRows * 16; idx += Cfg::kThreads) {
+    const int m = idx >> 4;
+    const int c = idx & 15;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (m < n_rows) {
+      const int i = m / Lc;
+      const int r = r0 + m % Lc;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const __nv_bfloat16*>(args.q) +
+          ((static_cast<size_t>(b) * args.Hq + g * kGroup + i) * args.L + r) * kHeadDim);
+      val = __ldg(src + c);
+    }
+    *reinterpret_cast<uint4*>(smem + Cfg::kQOff + (c >> 3) * Cfg::kQSlab + (m >> 3) * 1024 + (m & 7) * 128 +
+                              (((c & 7) ^ (m & 7)) << 4)) = val;
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Cfg::kNumBars; ++i) mbar_init(bar(i), i == Cfg::kBarPFull ? 32u : 1u);
+    for (int i = 0; i < Cfg::kNumBars; ++i)
+      mbar_init(bar(i), i == Cfg::kBarPFull ? static_cast<uint32_t>(32 * Cfg::kSoftmaxWarps) : 1u);
     misc[1] = (*reinterpret_cast<volatile uint32_t*>(args.err) != 0) ? 1u : 0u;
     fence_mbar_init();
   }
   fence_proxy_async_smem();   // generic-proxy Q writes -> visible to the tensor core
-  if (warp == 2) {
+  if (warp == Cfg::kMmaWarp) {
     tmem_alloc(sbase + Cfg::kMiscOff, Cfg::kTmemCols);
     tmem_relinquish();
   }
@@ -98,50 +152,80 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   const uint32_t tmem_base = misc[0];
   const bool skip = (*abort_flag != 0);
 
-  if (warp == 1) {
+  if (warp == Cfg::kProdWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && !skip) {
-      tma_prefetch_desc(&tmap_k);
-      tma_prefetch_desc(&tmap_v);
+    if (!skip) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+      }
       const uint64_t stream_once = l2_policy_evict_first();
-      const int z = b * args.Hkv + g;
       int issued = 0;
       bool ok = true;
       for (int j = 0; j < n_kv && ok; ++j) {
         const int slot = j % Cfg::kStages;
         const uint32_t use = j / Cfg::kStages;
+        int row = 0, plane = 0;
+        if (lane == 0) kv_tile_coords(args, b, g, j, row, plane);
         if (j >= Cfg::kStages)
           ok = mbar_wait(bar(Cfg::kBarKEmpty + slot), (use - 1) & 1, abort_flag, args.err, kDevTimeoutSlot);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        const uint32_t kdst = sbase + Cfg::kKOff + slot * kTileBytes;
-        mbar_arrive_expect_tx(bar(Cfg::kBarKFull + slot), kTileBytes);
-        tma_load_3d_hint(kdst, &tmap_k, 0, j * kTileKeys, z, bar(Cfg::kBarKFull + slot), stream_once);
-        tma_load_3d_hint(kdst + kSlabBytes, &tmap_k, 64, j * kTileKeys, z, bar(Cfg::kBarKFull + slot), stream_once);
+        if (lane == 0) {
+          const uint32_t kdst = sbase + Cfg::kKOff + slot * kTileBytes;
+          mbar_arrive_expect_tx(bar(Cfg::kBarKFull + slot), kTileBytes);
+          tma_load_3d_hint(kdst, &tmap_k, 0, row, plane, bar(Cfg::kBarKFull + slot), stream_once);
+          tma_load_3d_hint(kdst + kSlabBytes, &tmap_k, 64, row, plane, bar(Cfg::kBarKFull + slot), stream_once);
+        }
+        issued = 2 * j + 1;
         if (j >= Cfg::kStages)
           ok = mbar_wait(bar(Cfg::kBarVEmpty + slot), (use - 1) & 1, abort_flag, args.err, kDevTimeoutSlot);
-        if (!ok) { issued = 2 * j + 1; break; }
-        const uint32_t vdst = sbase + Cfg::kVOff + slot * kTileBytes;
-        mbar_arrive_expect_tx(bar(Cfg::kBarVFull + slot), kTileBytes);
-        tma_load_3d_hint(vdst, &tmap_v, 0, j * kTileKeys, z, bar(Cfg::kBarVFull + slot), stream_once);
-        tma_load_3d_hint(vdst + kSlabBytes, &tmap_v, 64, j * kTileKeys, z, bar(Cfg::kBarVFull + slot), stream_once);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t vdst = sbase + Cfg::kVOff + slot * kTileBytes;
+          mbar_arrive_expect_tx(bar(Cfg::kBarVFull + slot), kTileBytes);
+          tma_load_3d_hint(vdst, &tmap_v, 0, row, plane, bar(Cfg::kBarVFull + slot), stream_once);
+          tma_load_3d_hint(vdst + kSlabBytes, &tmap_v, 64, row, plane, bar(Cfg::kBarVFull + slot), stream_once);
+        }
         issued = 2 * j + 2;
       }
-      if (!ok) {
+      if (ok && zero_tail) {
+        // V rows past the sequence in its last tile may hold anything (another
+        // sequence's data, NaN): make them zero so P = 0 contributes nothing.
+        const int jl = n_kv - 1;
+        const int slot = jl % Cfg::kStages;
+        ok = mbar_wait(bar(Cfg::kBarVFull + slot), (jl / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          uint8_t* vt = smem + Cfg::kVOff + slot * kTileBytes;
+          for (int idx = tail_from * 16 + lane; idx < kTileKeys * 16; idx += 32) {
+            const int row = idx >> 4;
+            const int c = idx & 15;
+            *reinterpret_cast<uint4*>(vt + (c >> 3) * kSlabBytes + (row >> 3) * 1024 + (row & 7) * 128 +
+                                      (((c & 7) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(Cfg::kBarVReady));
+        }
+      }
+      if (!ok && lane == 0) {
         for (int x = (issued > 2 * Cfg::kStages ? issued - 2 * Cfg::kStages : 0); x < issued; ++x) {
           const int j = x >> 1;
-          decode_drain_wait(bar(((x & 1) ? Cfg::kBarVFull : Cfg::kBarKFull) + j % Cfg::kStages),
+          packed_drain_wait(bar(((x & 1) ? Cfg::kBarVFull : Cfg::kBarKFull) + j % Cfg::kStages),
                             (j / Cfg::kStages) & 1);
         }
       }
     }
-  } else if (warp == 2) {
+  } else if (warp == Cfg::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && !skip) {
       const uint32_t q_saddr = sbase + Cfg::kQOff;
       bool ok = mbar_wait(bar(Cfg::kBarKFull), 0, abort_flag, args.err, kDevTimeoutTma);
       if (ok) {
         tc_fence_after();
-        issue_qk(tmem_base, q_saddr, 0u, Cfg::kQAtom, sbase + Cfg::kKOff);
+        issue_qk(tmem_base, q_saddr, Cfg::kQSbo, Cfg::kQSlab, sbase + Cfg::kKOff);
         tc_commit(bar(Cfg::kBarSFull));
         tc_commit(bar(Cfg::kBarKEmpty));
       }
@@ -154,13 +238,20 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           if (ok && jn >= 2) ok = mbar_wait(bar(Cfg::kBarOFull), (j - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
           if (!ok) break;
           tc_fence_after();
-          issue_qk(tmem_base + (jn & 1) * 128u, q_saddr, 0u, Cfg::kQAtom, sbase + Cfg::kKOff + slot * kTileBytes);
+          issue_qk(tmem_base + (jn & 1) * 128u, q_saddr, Cfg::kQSbo, Cfg::kQSlab,
+                   sbase + Cfg::kKOff + slot * kTileBytes);
           tc_commit(bar(Cfg::kBarSFull + (jn & 1)));
           tc_commit(bar(Cfg::kBarKEmpty + slot));
         }
         const int slot = j % Cfg::kStages;
         ok = mbar_wait(bar(Cfg::kBarPFull), j & 1, abort_flag, args.err, kDevTimeoutSoftmax);
-        if (ok) ok = mbar_wait(bar(Cfg::kBarVFull + slot), (j / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+        if (ok) {
+          if (zero_tail && j == n_kv - 1)
+            ok = mbar_wait(bar(Cfg::kBarVReady), 0, abort_flag, args.err, kDevTimeoutTma);
+          else
+            ok = mbar_wait(bar(Cfg::kBarVFull + slot), (j / Cfg::kStages) & 1, abort_flag, args.err,
+                           kDevTimeoutTma);
+        }
         if (!ok) break;
         tc_fence_after();
         issue_pv(tmem_base + 256u, tmem_base + (j & 1) * 128u, sbase + Cfg::kVOff + slot * kTileBytes, j == 0);
@@ -169,12 +260,17 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       }
       if (!ok) {
         tc_commit(bar(Cfg::kBarDrain));
-        decode_drain_wait(bar(Cfg::kBarDrain), 0);
+        packed_drain_wait(bar(Cfg::kBarDrain), 0);
       }
     }
   } else {
     // ------------------------------------------------------------- softmax
-    const uint32_t o_tmem = tmem_base + 256u;   // warp 0: lanes 0..31, lane offset 0
+    const int m = warp * 32 + lane;                    // packed row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t o_tmem = tmem_base + 256u + lane_off;
+    const int head = (m < n_rows) ? m / Lc : 0;
+    const int r = (m < n_rows) ? r0 + m % Lc : r0;     // unused rows take the sub-chunk's first position
+    const int pos = pos0 + r;
     RowState st = row_state_init();
     bool ok = !skip;
     for (int j = 0; j < n_kv && ok; ++j) {
@@ -182,11 +278,11 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t s_tmem = tmem_base + (j & 1) * 128u;
+      const uint32_t s_tmem = tmem_base + (j & 1) * 128u + lane_off;
       uint32_t s[128];
       tmem_ld128_wait(s_tmem, s);
       uint32_t p[64];
-      const float alpha = (j == n_kv - 1) ? row_softmax_tile<true>(s, ctx - j * kTileKeys, st, p)
+      const float alpha = (j == n_kv - 1) ? row_softmax_tile<true>(s, pos - j * kTileKeys + 1, st, p)
                                           : row_softmax_tile<false>(s, kTileKeys, st, p);
       if (j > 0) {
         ok = mbar_wait(bar(Cfg::kBarOFull), (j - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
@@ -219,10 +315,10 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     if (ok) {
       tc_fence_after();
       const float inv_l = row_inv_l(st);
-      const bool store = lane < kGroup;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.o) +
-                                            (static_cast<size_t>(b) * args.Hq + g * kGroup + (store ? lane : 0)) *
-                                                kHeadDim);
+      const bool store = m < n_rows;
+      uint4* dst = reinterpret_cast<uint4*>(
+          static_cast<__nv_bfloat16*>(args.o) +
+          ((static_cast<size_t>(b) * args.Hq + g * kGroup + head) * args.L + r) * kHeadDim);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32], w[16];
@@ -239,27 +335,38 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == Cfg::kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
 }
 
-cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t s) {
-  static_assert(DecodeCfg::kSmemUsed <= 227u * 1024u, "shared memory budget");
+template <bool kWide>
+static cudaError_t launch_packed_t(const CUtensorMap& tk, const CUtensorMap& tv, const PackedArgs& a, int n_sub,
+                                   cudaStream_t s) {
+  using Cfg = PackedCfg<kWide>;
+  static_assert(Cfg::kSmemUsed <= 227u * 1024u, "shared memory budget");
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(kb_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(DecodeCfg::kSmemBytes));
+    e = cudaFuncSetAttribute(kb_decode_kernel<kWide>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Cfg::kSmemBytes));
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  kb_decode_kernel<<<static_cast<unsigned>(a.B * a.Hkv), DecodeCfg::kThreads, DecodeCfg::kSmemBytes, s>>>(tk, tv, a);
+  const unsigned grid = static_cast<unsigned>(n_sub * a.B * a.Hkv);
+  kb_decode_kernel<kWide><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(tk, tv, a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_packed(const CUtensorMap& tk, const CUtensorMap& tv, const PackedArgs& a, int n_sub,
+                          cudaStream_t s) {
+  // narrow when at most 8 rows are packed (two query rows per head)
+  if (a.L <= 2) return launch_packed_t<false>(tk, tv, a, n_sub, s);
+  return launch_packed_t<true>(tk, tv, a, n_sub, s);
 }
 
 // A kernel that waits on an mbarrier nobody ever signals, with a short limit:

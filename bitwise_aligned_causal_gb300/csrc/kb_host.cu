@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -113,7 +114,8 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   if (L < 1 || start < 0 || kv_cap < 1) return KB_ERR_INVALID_ARG;
   if (static_cast<long long>(start) + L > kv_cap) return KB_ERR_INVALID_ARG;
   if (kv_cap > kMaxRows) return KB_ERR_UNSUPPORTED;
-  if (q_tiles_per_cta != 1 && q_tiles_per_cta != 2) return KB_ERR_INVALID_ARG;
+  if (q_tiles_per_cta < 0 || q_tiles_per_cta > 2) return KB_ERR_INVALID_ARG;
+  if (q_tiles_per_cta == 0 && L > kb::kMaxPackedRows) return KB_ERR_INVALID_ARG;
   const int first_tile = start / kb::kTileRows;
   const int last_tile = (start + L - 1) / kb::kTileRows;
   const long long grid = static_cast<long long>(last_tile - first_tile + 1) * B * (Hq / q_tiles_per_cta);
@@ -126,10 +128,33 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
 
   CUtensorMap tq, tk, tv;
   const uint64_t row_bytes = kb::kHeadDim * 2u;
+  const uint64_t kv_len = static_cast<uint64_t>(start) + L;
+  if (q_tiles_per_cta == 0) {
+    // query rows packed by GQA group; the cache map ends at the chunk's last key
+    if ((s = encode_rows_map(&tk, k, kv_len, static_cast<uint64_t>(B) * Hkv,
+                             static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
+      return s;
+    if ((s = encode_rows_map(&tv, v, kv_len, static_cast<uint64_t>(B) * Hkv,
+                             static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
+      return s;
+    kb::PackedArgs a{};
+    a.q = q;
+    a.o = o;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.L = L;
+    a.start = start;
+    a.max_ctx = kv_cap;
+    a.err = dst->err;
+    const int split = std::min(L, kb::kTileKeys - start % kb::kTileKeys);
+    const cudaError_t e = kb::launch_packed(tk, tv, a, split < L ? 2 : 1, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return KB_OK;
+  }
   if ((s = encode_rows_map(&tq, q, static_cast<uint64_t>(L), static_cast<uint64_t>(B) * Hq,
                            static_cast<uint64_t>(L) * row_bytes)) != KB_OK)
     return s;
-  const uint64_t kv_len = static_cast<uint64_t>(start) + L;
   if ((s = encode_rows_map(&tk, k, kv_len, static_cast<uint64_t>(B) * Hkv,
                            static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
     return s;
@@ -154,13 +179,16 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
 
 constexpr int kDefaultQTilesPerCta = 1;
 
+// Chunks of at most this many query rows go to the packed kernel.
+int chunk_cta_shape(int L) { return L <= kb::kMaxPackedRows ? 0 : kDefaultQTilesPerCta; }
+
 }  // namespace
 
 extern "C" {
 
 kb_status kb_attn_chunk(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int L,
                         int start, int kv_cap, void* stream) {
-  return chunk_impl(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, kDefaultQTilesPerCta, stream);
+  return chunk_impl(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, chunk_cta_shape(L), stream);
 }
 
 kb_status kb_attn_chunk_cta_shape(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
@@ -171,7 +199,7 @@ kb_status kb_attn_chunk_cta_shape(const void* q, const void* k, const void* v, v
 kb_status kb_attn_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int S,
                           void* stream) {
   if (S < 1) return KB_ERR_INVALID_ARG;
-  return chunk_impl(q, k, v, o, B, Hq, Hkv, S, 0, S, kDefaultQTilesPerCta, stream);
+  return chunk_impl(q, k, v, o, B, Hq, Hkv, S, 0, S, chunk_cta_shape(S), stream);
 }
 
 kb_status kb_attn_decode(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int ctx_len,
@@ -181,29 +209,55 @@ kb_status kb_attn_decode(const void* q, const void* k, const void* v, void* o, i
   if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
   if (ctx_len < 1 || kv_cap < 1 || ctx_len > kv_cap) return KB_ERR_INVALID_ARG;
   if (kv_cap > kMaxRows) return KB_ERR_UNSUPPORTED;
+  // one query row at position ctx_len - 1: the packed chunk path with L = 1
+  return chunk_impl(q, k, v, o, B, Hq, Hkv, 1, ctx_len - 1, kv_cap, 0, stream);
+}
+
+kb_status kb_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o, int B, int Hq,
+                               int Hkv, const int* block_table, int pages_per_seq, int page_size, int num_pages,
+                               const int* ctx_lens, void* stream) {
+  kb_status s = check_ptrs(q, k_pages, v_pages, o);
+  if (s != KB_OK) return s;
+  if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
+  if (!block_table || !ctx_lens) return KB_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(ctx_lens) & 3u))
+    return KB_ERR_INVALID_ARG;
+  if (pages_per_seq < 1 || num_pages < 1 || page_size < kb::kTileKeys) return KB_ERR_INVALID_ARG;
+  if (page_size % kb::kTileKeys != 0) return KB_ERR_UNSUPPORTED;
+  if (static_cast<long long>(pages_per_seq) * page_size > kMaxRows) return KB_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_pages) * Hkv > 0x7FFFFFFFLL) return KB_ERR_UNSUPPORTED;
 
   DeviceState* dst = nullptr;
   if ((s = get_device_state(&dst)) != KB_OK) return s;
-  for (const void* p : {q, k, v, static_cast<const void*>(o)})
+  for (const void* p : {q, k_pages, v_pages, static_cast<const void*>(o), static_cast<const void*>(block_table),
+                        static_cast<const void*>(ctx_lens)})
     if ((s = check_device_pointer(p)) != KB_OK) return s;
 
+  // pools [num_pages, Hkv, page_size, 128]: plane = page * Hkv + kv head
   CUtensorMap tk, tv;
   const uint64_t row_bytes = kb::kHeadDim * 2u;
-  if ((s = encode_rows_map(&tk, k, static_cast<uint64_t>(ctx_len), static_cast<uint64_t>(B) * Hkv,
-                           static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
+  const uint64_t planes = static_cast<uint64_t>(num_pages) * Hkv;
+  if ((s = encode_rows_map(&tk, k_pages, static_cast<uint64_t>(page_size), planes,
+                           static_cast<uint64_t>(page_size) * row_bytes)) != KB_OK)
     return s;
-  if ((s = encode_rows_map(&tv, v, static_cast<uint64_t>(ctx_len), static_cast<uint64_t>(B) * Hkv,
-                           static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
+  if ((s = encode_rows_map(&tv, v_pages, static_cast<uint64_t>(page_size), planes,
+                           static_cast<uint64_t>(page_size) * row_bytes)) != KB_OK)
     return s;
-  kb::DecodeArgs a{};
+  kb::PackedArgs a{};
   a.q = q;
   a.o = o;
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
-  a.ctx = ctx_len;
+  a.L = 1;
+  a.ctx_lens = ctx_lens;
+  a.max_ctx = pages_per_seq * page_size;
+  a.block_table = block_table;
+  a.pages_per_seq = pages_per_seq;
+  a.page_size = page_size;
+  a.num_pages = num_pages;
   a.err = dst->err;
-  const cudaError_t e = kb::launch_decode(tk, tv, a, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = kb::launch_packed(tk, tv, a, 1, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return KB_OK;
 }
@@ -219,7 +273,7 @@ kb_status kb_attn_check_device_status(void* stream) {
   if (word != 0) {
     const uint32_t zero = 0;
     if ((e = cudaMemcpy(dst->err, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess) return cuda_fail(e);
-    return KB_ERR_TIMEOUT;
+    return word >= kb::kDevBadInput ? KB_ERR_INVALID_ARG : KB_ERR_TIMEOUT;
   }
   return KB_OK;
 }

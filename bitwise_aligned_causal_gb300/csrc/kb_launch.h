@@ -18,19 +18,29 @@ struct PrefillArgs {
   uint32_t* err;    // device error word
 };
 
-struct DecodeArgs {
-  const void* q;    // [B, Hq, 1, 128] bf16
-  void* o;          // [B, Hq, 1, 128] bf16
+// Query rows packed by GQA group (decode and chunks of at most 32 rows).
+struct PackedArgs {
+  const void* q;           // [B, Hq, L, 128] bf16
+  void* o;                 // [B, Hq, L, 128] bf16
   int B, Hq, Hkv;
-  int ctx;          // keys 0..ctx-1 are visible; the query sits at ctx-1
+  int L;                   // query rows per (batch, head)
+  int start;               // absolute position of query row 0 (when ctx_lens is null)
+  const int* ctx_lens;     // optional device [B]: row L-1 of batch b sits at ctx_lens[b] - 1
+  int max_ctx;             // largest valid ctx_lens entry (cache capacity)
+  const int* block_table;  // optional device [B, pages_per_seq]: paged K/V pools
+  int pages_per_seq, page_size, num_pages;
   uint32_t* err;
 };
+
+constexpr int kMaxPackedRows = 32;   // query rows per (batch, head) the packed kernel takes
 
 // Query tiles per CTA of the prefill kernel: 1 (two CTAs per SM) or 2
 // (two heads of one GQA group share every K/V tile).
 cudaError_t launch_prefill(int q_tiles_per_cta, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillArgs& a, cudaStream_t s);
-cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t s);
+// n_sub: 1, or 2 when the chunk crosses a 128-position tile boundary.
+cudaError_t launch_packed(const CUtensorMap& tk, const CUtensorMap& tv, const PackedArgs& a, int n_sub,
+                          cudaStream_t s);
 cudaError_t launch_wait_probe(uint32_t* err, unsigned long long limit_ns, cudaStream_t s);
 
 }  // namespace kb

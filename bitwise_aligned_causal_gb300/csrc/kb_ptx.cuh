@@ -18,10 +18,8 @@
 
 namespace kb {
 
-// Device-side error word: 0 = fine, otherwise the first error code recorded.
-// Defined in kb_host.cu (relocatable device code is not used, so each
-// translation unit that launches kernels gets its own copy via this
-// declaration being `static`).
+// Codes of the device-side error word (0 = fine; the first code recorded
+// wins).  The word lives in kb_host.cu; kernels get its address.
 enum DevError : uint32_t {
   kDevOk = 0,
   kDevTimeoutTma = 1,     // waited too long for a TMA tile
@@ -29,6 +27,7 @@ enum DevError : uint32_t {
   kDevTimeoutSoftmax = 3, // waited too long for the softmax warps
   kDevTimeoutSlot = 4,    // producer waited too long for a free slot
   kDevTimeoutProbe = 5,   // the deliberate timeout probe
+  kDevBadInput = 16,      // a device-resident argument (context length, page index) was out of range
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -230,6 +229,21 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
       : "memory");
 }
 
+// 64 consecutive columns, two loads then one wait.
+__device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : KB_R8(0), KB_R8(8), KB_R8(16), KB_R8(24), KB_R8(32), KB_R8(40), KB_R8(48), KB_R8(56)
+      : "r"(taddr), "r"(taddr + 32u)
+      : "memory");
+}
+
 // 128 consecutive columns, four loads then one wait.
 __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, uint32_t (&r)[128]) {
   asm volatile(
@@ -266,6 +280,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 }
 #undef KB_V8
 
+#define KB_V8(b) "r"(v[b + 0]), "r"(v[b + 1]), "r"(v[b + 2]), "r"(v[b + 3]), \
+                 "r"(v[b + 4]), "r"(v[b + 5]), "r"(v[b + 6]), "r"(v[b + 7])
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), KB_V8(0), KB_V8(8)
+      : "memory");
+}
+#undef KB_V8
+
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -286,6 +311,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+// Named barrier over `nthreads` threads (a multiple of 32); id 0 is __syncthreads.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0; }
 

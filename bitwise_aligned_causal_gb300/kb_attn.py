@@ -33,6 +33,7 @@ _SIGS = {
     "kb_attn_prefill": [_P, _P, _P, _P, _I, _I, _I, _I, _P],
     "kb_attn_chunk": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
     "kb_attn_decode": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
+    "kb_attn_decode_paged": [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _P, _P],
     "kb_attn_check_device_status": [_P],
     "kb_attn_debug_wait_timeout": [_I, _P],
     "kb_attn_chunk_cta_shape": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P],
@@ -86,6 +87,12 @@ def kb_attn_chunk(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, stream=None) -> int:
 
 def kb_attn_decode(q, k, v, o, B, Hq, Hkv, ctx_len, kv_cap, stream=None) -> int:
     return _lib.kb_attn_decode(q, k, v, o, B, Hq, Hkv, ctx_len, kv_cap, stream)
+
+
+def kb_attn_decode_paged(q, k_pages, v_pages, o, B, Hq, Hkv, block_table, pages_per_seq, page_size, num_pages,
+                         ctx_lens, stream=None) -> int:
+    return _lib.kb_attn_decode_paged(q, k_pages, v_pages, o, B, Hq, Hkv, block_table, pages_per_seq, page_size,
+                                     num_pages, ctx_lens, stream)
 
 
 def kb_attn_chunk_cta_shape(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, q_tiles_per_cta, stream=None) -> int:
@@ -172,6 +179,25 @@ def decode(q, k, v, ctx_len, out=None, stream=None):
     _check(o, "out", 4)
     _raise(kb_attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, int(ctx_len), cap,
                           _stream(stream)), "kb_attn_decode")
+    return o
+
+
+def decode_paged(q, k_pages, v_pages, block_table, ctx_lens, out=None, stream=None):
+    """Paged decode: q [B,Hq,1,128]; pools [num_pages,Hkv,page_size,128]; block_table int32 [B,pages_per_seq];
+    ctx_lens int32 [B] (all on the device)."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages")):
+        _check(t, n, 4)
+    for t, n in ((block_table, "block_table"), (ctx_lens, "ctx_lens")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+            raise TypeError(f"{n} must be a contiguous int32 CUDA tensor")
+    B, Hq = q.shape[0], q.shape[1]
+    num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    o = torch.empty_like(q) if out is None else out
+    _check(o, "out", 4)
+    _raise(kb_attn_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), o.data_ptr(), B, Hq, Hkv,
+                                block_table.data_ptr(), block_table.shape[1], page_size, num_pages,
+                                ctx_lens.data_ptr(), _stream(stream)), "kb_attn_decode_paged")
     return o
 
 

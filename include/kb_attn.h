@@ -76,10 +76,31 @@ kb_status kb_attn_decode(const void* q, const void* k, const void* v, void* o,
                          int B, int Hq, int Hkv, int ctx_len, int kv_cap, void* stream);
 
 /*
+ * One-token decode over a paged KV cache, one context length per sequence
+ * (README "Usage": unified_decode; the page table is this library's
+ * addition, the pages show only a contiguous cache).
+ *   q, o         : [B, Hq, 1, 128]; the query of batch b sits at position ctx_lens[b] - 1
+ *   k_pages,
+ *   v_pages      : pools [num_pages, Hkv, page_size, 128] bf16
+ *   block_table  : device int32 [B, pages_per_seq]; key position p of batch b lives in
+ *                  page block_table[b, p / page_size] at row p % page_size
+ *   ctx_lens     : device int32 [B], each in 1 .. pages_per_seq * page_size
+ * page_size must be a positive multiple of 128.  Page rows past a sequence's
+ * context may hold anything.  Bits equal kb_attn_decode on the same keys and
+ * values laid out contiguously.  Out-of-range ctx_lens or page indices are
+ * found on the device: the affected rows are not written and the next
+ * kb_attn_check_device_status returns KB_ERR_INVALID_ARG.
+ */
+kb_status kb_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, void* o,
+                               int B, int Hq, int Hkv, const int* block_table, int pages_per_seq,
+                               int page_size, int num_pages, const int* ctx_lens, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device-side
  * error word on the current device.  Returns KB_ERR_TIMEOUT if any kernel
  * since the last check gave up on a bounded wait (its output is then
- * undefined), KB_ERR_CUDA if the synchronisation failed, else KB_OK.
+ * undefined), KB_ERR_INVALID_ARG if a kernel found a device-resident argument
+ * out of range, KB_ERR_CUDA if the synchronisation failed, else KB_OK.
  */
 kb_status kb_attn_check_device_status(void* stream);
 
@@ -92,9 +113,12 @@ kb_status kb_attn_check_device_status(void* stream);
 kb_status kb_attn_debug_wait_timeout(int limit_us, void* stream);
 
 /*
- * Prefill/chunk with an explicit CTA shape, for tests of the contract: the
- * kernel runs q_tiles_per_cta (1 or 2) query tiles per CTA.  Both shapes give
- * the same bits as kb_attn_chunk.
+ * Prefill/chunk with an explicit kernel shape, for tests of the contract:
+ * q_tiles_per_cta = 1 or 2 runs the tile kernel with that many 128-row query
+ * tiles per CTA; 0 runs the packed kernel (the 4 heads of a GQA group times
+ * the chunk's rows in one MMA tile; L <= 32).  kb_attn_chunk, kb_attn_prefill
+ * and kb_attn_decode pick packed for L <= 32 and 1 otherwise.  Every shape
+ * gives the same bits.
  */
 kb_status kb_attn_chunk_cta_shape(const void* q, const void* k, const void* v, void* o,
                                   int B, int Hq, int Hkv, int L, int start, int kv_cap,

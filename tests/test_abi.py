@@ -77,3 +77,20 @@ def test_bad_sizes_rejected(kb):
     assert kb.kb_attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 0, 10) == kb.KB_ERR_INVALID_ARG
     assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 4, 0, 10, 3) == kb.KB_ERR_INVALID_ARG
     assert kb.kb_attn_debug_wait_timeout(0) == kb.KB_ERR_INVALID_ARG
+
+
+def test_paged_decode_arguments_rejected(kb):
+    ok = (FAKE, FAKE, FAKE, FAKE, 2, 32, 8)
+    assert kb.kb_attn_decode_paged(*ok, None, 4, 128, 10, FAKE) == kb.KB_ERR_INVALID_ARG      # no block table
+    assert kb.kb_attn_decode_paged(*ok, FAKE, 4, 128, 10, None) == kb.KB_ERR_INVALID_ARG      # no ctx_lens
+    assert kb.kb_attn_decode_paged(*ok, FAKE + 2, 4, 128, 10, FAKE) == kb.KB_ERR_INVALID_ARG  # misaligned table
+    assert kb.kb_attn_decode_paged(*ok, FAKE, 4, 64, 10, FAKE) == kb.KB_ERR_INVALID_ARG       # page < 128 keys
+    assert kb.kb_attn_decode_paged(*ok, FAKE, 4, 192, 10, FAKE) == kb.KB_ERR_UNSUPPORTED      # not a multiple of 128
+    assert kb.kb_attn_decode_paged(*ok, FAKE, 0, 128, 10, FAKE) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_decode_paged(*ok, FAKE, 4, 128, 0, FAKE) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_decode_paged(FAKE, FAKE, FAKE, FAKE, 2, 32, 4, FAKE, 4, 128, 10, FAKE) == kb.KB_ERR_UNSUPPORTED
+
+
+def test_packed_shape_limits(kb):
+    assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 33, 0, 64, 0) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 4, 0, 64, -1) == kb.KB_ERR_INVALID_ARG
