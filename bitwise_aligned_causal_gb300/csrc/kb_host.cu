@@ -106,8 +106,23 @@ kb_status check_ptrs(const void* q, const void* k, const void* v, const void* o)
   return KB_OK;
 }
 
+// A paged K/V pool [num_pages, Hkv, page_size, 128] and its page table.
+struct Paging {
+  const int* block_table = nullptr;  // device [B, pages_per_seq]
+  int pages_per_seq = 0, page_size = 0, num_pages = 0;
+};
+
+kb_status check_paging(const Paging& pg, int Hkv) {
+  if (!pg.block_table || (reinterpret_cast<uintptr_t>(pg.block_table) & 3u)) return KB_ERR_INVALID_ARG;
+  if (pg.pages_per_seq < 1 || pg.num_pages < 1 || pg.page_size < kb::kTileKeys) return KB_ERR_INVALID_ARG;
+  if (pg.page_size % kb::kTileKeys != 0) return KB_ERR_UNSUPPORTED;
+  if (static_cast<long long>(pg.pages_per_seq) * pg.page_size > kMaxRows) return KB_ERR_UNSUPPORTED;
+  if (static_cast<long long>(pg.num_pages) * Hkv > 0x7FFFFFFFLL) return KB_ERR_UNSUPPORTED;
+  return KB_OK;
+}
+
 kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int L, int start,
-                     int kv_cap, int q_tiles_per_cta, void* stream) {
+                     int kv_cap, int q_tiles_per_cta, void* stream, const Paging* paging = nullptr) {
   kb_status s = check_ptrs(q, k, v, o);
   if (s != KB_OK) return s;
   if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
@@ -118,25 +133,33 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   if (q_tiles_per_cta == 0 && L > kb::kMaxPackedRows) return KB_ERR_INVALID_ARG;
   const int first_tile = start / kb::kTileRows;
   const int last_tile = (start + L - 1) / kb::kTileRows;
-  const long long grid = static_cast<long long>(last_tile - first_tile + 1) * B * (Hq / q_tiles_per_cta);
+  // CTAs: tile kernel one per (query tile, batch, head group); packed kernel
+  // at most two per (batch, KV head)
+  const long long grid = q_tiles_per_cta > 0
+                             ? static_cast<long long>(last_tile - first_tile + 1) * B * (Hq / q_tiles_per_cta)
+                             : 2LL * B * Hkv;
   if (grid > 0x7FFFFFFFLL) return KB_ERR_UNSUPPORTED;
 
   DeviceState* dst = nullptr;
   if ((s = get_device_state(&dst)) != KB_OK) return s;
   for (const void* p : {q, k, v, static_cast<const void*>(o)})
     if ((s = check_device_pointer(p)) != KB_OK) return s;
+  if (paging && (s = check_device_pointer(paging->block_table)) != KB_OK) return s;
 
   CUtensorMap tq, tk, tv;
   const uint64_t row_bytes = kb::kHeadDim * 2u;
   const uint64_t kv_len = static_cast<uint64_t>(start) + L;
+  // K/V maps: a contiguous cache ends at the chunk's last key (later rows read
+  // as zeros); a paged pool is [num_pages * Hkv planes, page_size rows].
+  const uint64_t kv_rows = paging ? static_cast<uint64_t>(paging->page_size) : kv_len;
+  const uint64_t kv_planes =
+      paging ? static_cast<uint64_t>(paging->num_pages) * Hkv : static_cast<uint64_t>(B) * Hkv;
+  const uint64_t kv_stride = (paging ? static_cast<uint64_t>(paging->page_size) : static_cast<uint64_t>(kv_cap)) *
+                             row_bytes;
+  if ((s = encode_rows_map(&tk, k, kv_rows, kv_planes, kv_stride)) != KB_OK) return s;
+  if ((s = encode_rows_map(&tv, v, kv_rows, kv_planes, kv_stride)) != KB_OK) return s;
   if (q_tiles_per_cta == 0) {
-    // query rows packed by GQA group; the cache map ends at the chunk's last key
-    if ((s = encode_rows_map(&tk, k, kv_len, static_cast<uint64_t>(B) * Hkv,
-                             static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
-      return s;
-    if ((s = encode_rows_map(&tv, v, kv_len, static_cast<uint64_t>(B) * Hkv,
-                             static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
-      return s;
+    // query rows packed by GQA group
     kb::PackedArgs a{};
     a.q = q;
     a.o = o;
@@ -146,6 +169,12 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
     a.L = L;
     a.start = start;
     a.max_ctx = kv_cap;
+    if (paging) {
+      a.block_table = paging->block_table;
+      a.pages_per_seq = paging->pages_per_seq;
+      a.page_size = paging->page_size;
+      a.num_pages = paging->num_pages;
+    }
     a.err = dst->err;
     const int split = std::min(L, kb::kTileKeys - start % kb::kTileKeys);
     const cudaError_t e = kb::launch_packed(tk, tv, a, split < L ? 2 : 1, static_cast<cudaStream_t>(stream));
@@ -154,12 +183,6 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   }
   if ((s = encode_rows_map(&tq, q, static_cast<uint64_t>(L), static_cast<uint64_t>(B) * Hq,
                            static_cast<uint64_t>(L) * row_bytes)) != KB_OK)
-    return s;
-  if ((s = encode_rows_map(&tk, k, kv_len, static_cast<uint64_t>(B) * Hkv,
-                           static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
-    return s;
-  if ((s = encode_rows_map(&tv, v, kv_len, static_cast<uint64_t>(B) * Hkv,
-                           static_cast<uint64_t>(kv_cap) * row_bytes)) != KB_OK)
     return s;
 
   kb::PrefillArgs a{};
@@ -171,6 +194,12 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   a.start = start;
   a.first_tile = first_tile;
   a.n_tiles = last_tile - first_tile + 1;
+  if (paging) {
+    a.block_table = paging->block_table;
+    a.pages_per_seq = paging->pages_per_seq;
+    a.page_size = paging->page_size;
+    a.num_pages = paging->num_pages;
+  }
   a.err = dst->err;
   const cudaError_t e = kb::launch_prefill(q_tiles_per_cta, tq, tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
@@ -202,6 +231,22 @@ kb_status kb_attn_prefill(const void* q, const void* k, const void* v, void* o, 
   return chunk_impl(q, k, v, o, B, Hq, Hkv, S, 0, S, chunk_cta_shape(S), stream);
 }
 
+kb_status kb_attn_chunk_paged(const void* q, const void* k_pages, const void* v_pages, void* o, int B, int Hq,
+                              int Hkv, int L, int start, const int* block_table, int pages_per_seq, int page_size,
+                              int num_pages, void* stream) {
+  Paging pg;
+  pg.block_table = block_table;
+  pg.pages_per_seq = pages_per_seq;
+  pg.page_size = page_size;
+  pg.num_pages = num_pages;
+  kb_status s = check_heads(B, Hq, Hkv);
+  if (s != KB_OK) return s;
+  if ((s = check_paging(pg, Hkv)) != KB_OK) return s;
+  const long long cap = static_cast<long long>(pages_per_seq) * page_size;
+  return chunk_impl(q, k_pages, v_pages, o, B, Hq, Hkv, L, start, static_cast<int>(cap), chunk_cta_shape(L), stream,
+                    &pg);
+}
+
 kb_status kb_attn_decode(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int ctx_len,
                          int kv_cap, void* stream) {
   kb_status s = check_ptrs(q, k, v, o);
@@ -219,13 +264,13 @@ kb_status kb_attn_decode_paged(const void* q, const void* k_pages, const void* v
   kb_status s = check_ptrs(q, k_pages, v_pages, o);
   if (s != KB_OK) return s;
   if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
-  if (!block_table || !ctx_lens) return KB_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(ctx_lens) & 3u))
-    return KB_ERR_INVALID_ARG;
-  if (pages_per_seq < 1 || num_pages < 1 || page_size < kb::kTileKeys) return KB_ERR_INVALID_ARG;
-  if (page_size % kb::kTileKeys != 0) return KB_ERR_UNSUPPORTED;
-  if (static_cast<long long>(pages_per_seq) * page_size > kMaxRows) return KB_ERR_UNSUPPORTED;
-  if (static_cast<long long>(num_pages) * Hkv > 0x7FFFFFFFLL) return KB_ERR_UNSUPPORTED;
+  if (!ctx_lens || (reinterpret_cast<uintptr_t>(ctx_lens) & 3u)) return KB_ERR_INVALID_ARG;
+  Paging pg;
+  pg.block_table = block_table;
+  pg.pages_per_seq = pages_per_seq;
+  pg.page_size = page_size;
+  pg.num_pages = num_pages;
+  if ((s = check_paging(pg, Hkv)) != KB_OK) return s;
 
   DeviceState* dst = nullptr;
   if ((s = get_device_state(&dst)) != KB_OK) return s;

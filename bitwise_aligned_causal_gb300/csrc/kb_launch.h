@@ -15,6 +15,8 @@ struct PrefillArgs {
   int start;        // absolute position of query row 0
   int first_tile;   // floor(start / 128)
   int n_tiles;      // absolute query tiles touched by [start, start+L)
+  const int* block_table;  // optional device [B, pages_per_seq]: paged K/V pools
+  int pages_per_seq, page_size, num_pages;
   uint32_t* err;    // device error word
 };
 

@@ -43,7 +43,8 @@ struct PrefillCfg {
   static constexpr int kBarSFull = kBarVEmpty + kStages;
   static constexpr int kBarPFull = kBarSFull + NQ;
   static constexpr int kBarOFull = kBarPFull + NQ;
-  static constexpr int kBarDrain = kBarOFull + NQ;
+  static constexpr int kBarVReady = kBarOFull + NQ;         // last V tile with its tail zeroed (paged)
+  static constexpr int kBarDrain = kBarVReady + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // [0] tmem base, [1] abort flag
   static constexpr uint32_t kSmemUsed = kMiscOff + 16;
@@ -105,44 +106,86 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
   const uint32_t tmem_base = misc[0];
   const bool skip = (*abort_flag != 0);
 
+  const bool paged = args.block_table != nullptr;
+  const int kv_len = args.start + args.L;                          // keys at or beyond kv_len are never used
   if (warp == Cfg::kLoadWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && !skip) {
-      tma_prefetch_desc(&tmap_q);
-      tma_prefetch_desc(&tmap_k);
-      tma_prefetch_desc(&tmap_v);
+    if (!skip) {
       const uint64_t keep = l2_policy_evict_last();
-      const int yq = t * kTileRows - args.start;      // may be negative: zero-filled rows
-      mbar_arrive_expect_tx(bar(Cfg::kBarQFull), NQ * kTileBytes);
-      for (int qi = 0; qi < NQ; ++qi) {
-        const int zq = b * args.Hq + h0 + qi;
-        const uint32_t dst = sbase + Cfg::kQOff + qi * kTileBytes;
-        tma_load_3d(dst, &tmap_q, 0, yq, zq, bar(Cfg::kBarQFull));
-        tma_load_3d(dst + kSlabBytes, &tmap_q, 64, yq, zq, bar(Cfg::kBarQFull));
+      if (lane == 0) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+        const int yq = t * kTileRows - args.start;      // may be negative: zero-filled rows
+        mbar_arrive_expect_tx(bar(Cfg::kBarQFull), NQ * kTileBytes);
+        for (int qi = 0; qi < NQ; ++qi) {
+          const int zq = b * args.Hq + h0 + qi;
+          const uint32_t dst = sbase + Cfg::kQOff + qi * kTileBytes;
+          tma_load_3d(dst, &tmap_q, 0, yq, zq, bar(Cfg::kBarQFull));
+          tma_load_3d(dst + kSlabBytes, &tmap_q, 64, yq, zq, bar(Cfg::kBarQFull));
+        }
       }
-      const int zkv = b * args.Hkv + g;
       int issued = 0;
       bool ok = true;
       for (int j = 0; j < n_kv && ok; ++j) {
         const int slot = j % Cfg::kStages;
         const uint32_t use = j / Cfg::kStages;
+        // key tile j: rows of the K/V map and plane (a page of a paged pool)
+        int row = j * kTileKeys, plane = b * args.Hkv + g;
+        if (paged && lane == 0) {
+          int pg = args.block_table[static_cast<size_t>(b) * args.pages_per_seq + row / args.page_size];
+          if (pg < 0 || pg >= args.num_pages) {
+            atomicCAS(args.err, 0u, static_cast<uint32_t>(kDevBadInput));
+            pg = args.num_pages;       // beyond the map: the TMA unit reads zeros
+          }
+          row = row % args.page_size;
+          plane = pg * args.Hkv + g;
+        }
         if (j >= Cfg::kStages)
           ok = mbar_wait(bar(Cfg::kBarKEmpty + slot), (use - 1) & 1, abort_flag, args.err, kDevTimeoutSlot);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        const uint32_t kdst = sbase + Cfg::kKOff + slot * kTileBytes;
-        mbar_arrive_expect_tx(bar(Cfg::kBarKFull + slot), kTileBytes);
-        tma_load_3d_hint(kdst, &tmap_k, 0, j * kTileKeys, zkv, bar(Cfg::kBarKFull + slot), keep);
-        tma_load_3d_hint(kdst + kSlabBytes, &tmap_k, 64, j * kTileKeys, zkv, bar(Cfg::kBarKFull + slot), keep);
+        if (lane == 0) {
+          const uint32_t kdst = sbase + Cfg::kKOff + slot * kTileBytes;
+          mbar_arrive_expect_tx(bar(Cfg::kBarKFull + slot), kTileBytes);
+          tma_load_3d_hint(kdst, &tmap_k, 0, row, plane, bar(Cfg::kBarKFull + slot), keep);
+          tma_load_3d_hint(kdst + kSlabBytes, &tmap_k, 64, row, plane, bar(Cfg::kBarKFull + slot), keep);
+        }
+        issued = 2 * j + 1;
         if (j >= Cfg::kStages)
           ok = mbar_wait(bar(Cfg::kBarVEmpty + slot), (use - 1) & 1, abort_flag, args.err, kDevTimeoutSlot);
-        if (!ok) { issued = 2 * j + 1; break; }
-        const uint32_t vdst = sbase + Cfg::kVOff + slot * kTileBytes;
-        mbar_arrive_expect_tx(bar(Cfg::kBarVFull + slot), kTileBytes);
-        tma_load_3d_hint(vdst, &tmap_v, 0, j * kTileKeys, zkv, bar(Cfg::kBarVFull + slot), keep);
-        tma_load_3d_hint(vdst + kSlabBytes, &tmap_v, 64, j * kTileKeys, zkv, bar(Cfg::kBarVFull + slot), keep);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t vdst = sbase + Cfg::kVOff + slot * kTileBytes;
+          mbar_arrive_expect_tx(bar(Cfg::kBarVFull + slot), kTileBytes);
+          tma_load_3d_hint(vdst, &tmap_v, 0, row, plane, bar(Cfg::kBarVFull + slot), keep);
+          tma_load_3d_hint(vdst + kSlabBytes, &tmap_v, 64, row, plane, bar(Cfg::kBarVFull + slot), keep);
+        }
         issued = 2 * j + 2;
       }
-      if (!ok) {
+      if (ok && paged) {
+        // V rows past kv_len in the last tile belong to the page's unused
+        // part and may hold anything (NaN): zero them so P = 0 adds nothing.
+        const int jl = n_kv - 1;
+        const int slot = jl % Cfg::kStages;
+        ok = mbar_wait(bar(Cfg::kBarVFull + slot), (jl / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          uint8_t* vt = smem + Cfg::kVOff + slot * kTileBytes;
+          const int tail_from = min(kTileKeys, kv_len - jl * kTileKeys);
+          for (int idx = tail_from * 16 + lane; idx < kTileKeys * 16; idx += 32) {
+            const int vr = idx >> 4;
+            const int c = idx & 15;
+            *reinterpret_cast<uint4*>(vt + (c >> 3) * kSlabBytes + (vr >> 3) * 1024 + (vr & 7) * 128 +
+                                      (((c & 7) ^ (vr & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(Cfg::kBarVReady));
+        }
+      }
+      if (!ok && lane == 0) {
         // let every copy already issued land before shared memory is released
         drain_wait(bar(Cfg::kBarQFull), 0);
         for (int x = (issued > 2 * Cfg::kStages ? issued - 2 * Cfg::kStages : 0); x < issued; ++x) {
@@ -174,7 +217,10 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
       for (int j = 0; j < n_kv && ok; ++j) {
         const int slot = j % Cfg::kStages;
         const int nslot = (j + 1) % Cfg::kStages;
-        ok = mbar_wait(bar(Cfg::kBarVFull + slot), (j / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+        if (paged && j == n_kv - 1)
+          ok = mbar_wait(bar(Cfg::kBarVReady), 0, abort_flag, args.err, kDevTimeoutTma);
+        else
+          ok = mbar_wait(bar(Cfg::kBarVFull + slot), (j / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
         for (int qi = 0; qi < NQ && ok; ++qi) {
           ok = mbar_wait(bar(Cfg::kBarPFull + qi), j & 1, abort_flag, args.err, kDevTimeoutSoftmax);
           if (!ok) break;

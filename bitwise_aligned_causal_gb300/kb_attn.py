@@ -34,6 +34,7 @@ _SIGS = {
     "kb_attn_chunk": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
     "kb_attn_decode": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
     "kb_attn_decode_paged": [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _P, _P],
+    "kb_attn_chunk_paged": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _I, _I, _P],
     "kb_attn_check_device_status": [_P],
     "kb_attn_debug_wait_timeout": [_I, _P],
     "kb_attn_chunk_cta_shape": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P],
@@ -93,6 +94,12 @@ def kb_attn_decode_paged(q, k_pages, v_pages, o, B, Hq, Hkv, block_table, pages_
                          ctx_lens, stream=None) -> int:
     return _lib.kb_attn_decode_paged(q, k_pages, v_pages, o, B, Hq, Hkv, block_table, pages_per_seq, page_size,
                                      num_pages, ctx_lens, stream)
+
+
+def kb_attn_chunk_paged(q, k_pages, v_pages, o, B, Hq, Hkv, L, start, block_table, pages_per_seq, page_size,
+                        num_pages, stream=None) -> int:
+    return _lib.kb_attn_chunk_paged(q, k_pages, v_pages, o, B, Hq, Hkv, L, start, block_table, pages_per_seq,
+                                    page_size, num_pages, stream)
 
 
 def kb_attn_chunk_cta_shape(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, q_tiles_per_cta, stream=None) -> int:
@@ -198,6 +205,24 @@ def decode_paged(q, k_pages, v_pages, block_table, ctx_lens, out=None, stream=No
     _raise(kb_attn_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), o.data_ptr(), B, Hq, Hkv,
                                 block_table.data_ptr(), block_table.shape[1], page_size, num_pages,
                                 ctx_lens.data_ptr(), _stream(stream)), "kb_attn_decode_paged")
+    return o
+
+
+def chunk_paged(q, k_pages, v_pages, block_table, start, out=None, stream=None):
+    """Chunked forward over a paged cache: q [B,Hq,L,128] at positions start..; pools
+    [num_pages,Hkv,page_size,128]; block_table int32 [B,pages_per_seq] on the device."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages")):
+        _check(t, n, 4)
+    if not isinstance(block_table, torch.Tensor) or not block_table.is_cuda or block_table.dtype != torch.int32:
+        raise TypeError("block_table must be an int32 CUDA tensor")
+    B, Hq, L = q.shape[0], q.shape[1], q.shape[2]
+    num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    o = torch.empty_like(q) if out is None else out
+    _check(o, "out", 4)
+    _raise(kb_attn_chunk_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), o.data_ptr(), B, Hq, Hkv, L,
+                               int(start), block_table.data_ptr(), block_table.shape[1], page_size, num_pages,
+                               _stream(stream)), "kb_attn_chunk_paged")
     return o
 
 

@@ -76,6 +76,26 @@ kb_status kb_attn_decode(const void* q, const void* k, const void* v, void* o,
                          int B, int Hq, int Hkv, int ctx_len, int kv_cap, void* stream);
 
 /*
+ * Partitioned (chunked) forward against a paged KV cache: as kb_attn_chunk,
+ * with the keys and values of every sequence in pages of a shared pool (the
+ * page table is this library's addition; the pages show only a contiguous
+ * cache).
+ *   q, o         : [B, Hq, L, 128]; query row i is absolute position start + i
+ *   k_pages,
+ *   v_pages      : pools [num_pages, Hkv, page_size, 128] bf16; positions
+ *                  0..start+L-1 of every sequence must be written
+ *   block_table  : device int32 [B, pages_per_seq]; key position p of batch b
+ *                  lives in page block_table[b, p / page_size], row p % page_size
+ * page_size must be a positive multiple of 128; start + L <= pages_per_seq *
+ * page_size.  Bits equal kb_attn_chunk on the same data laid out contiguously.
+ * An out-of-range page index is found on the device and reported by the next
+ * kb_attn_check_device_status as KB_ERR_INVALID_ARG.
+ */
+kb_status kb_attn_chunk_paged(const void* q, const void* k_pages, const void* v_pages, void* o,
+                              int B, int Hq, int Hkv, int L, int start, const int* block_table,
+                              int pages_per_seq, int page_size, int num_pages, void* stream);
+
+/*
  * One-token decode over a paged KV cache, one context length per sequence
  * (README "Usage": unified_decode; the page table is this library's
  * addition, the pages show only a contiguous cache).

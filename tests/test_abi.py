@@ -94,3 +94,20 @@ def test_paged_decode_arguments_rejected(kb):
 def test_packed_shape_limits(kb):
     assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 33, 0, 64, 0) == kb.KB_ERR_INVALID_ARG
     assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 4, 0, 64, -1) == kb.KB_ERR_INVALID_ARG
+
+
+def test_paged_chunk_arguments_rejected(kb):
+    args = (FAKE, FAKE, FAKE, FAKE, 1, 32, 8)
+    assert kb.kb_attn_chunk_paged(*args, 16, 0, None, 4, 128, 8) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_chunk_paged(*args, 16, 500, FAKE, 4, 128, 8) == kb.KB_ERR_INVALID_ARG   # past 4 pages
+    assert kb.kb_attn_chunk_paged(*args, 16, 0, FAKE, 4, 100, 8) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_chunk_paged(*args, 16, 0, FAKE, 4, 192, 8) == kb.KB_ERR_UNSUPPORTED
+
+
+def test_packed_path_host_checks_do_not_trap(kb):
+    """Small chunks take the packed path; its host checks run without a GPU
+    and end in a CUDA error here (no device), never in a host fault."""
+    st = kb.kb_attn_chunk_paged(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 16, 0, FAKE, 4, 640, 8)
+    assert st in (kb.KB_ERR_CUDA, kb.KB_ERR_INVALID_ARG)
+    st = kb.kb_attn_chunk(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 16, 0, 64)
+    assert st in (kb.KB_ERR_CUDA, kb.KB_ERR_INVALID_ARG)

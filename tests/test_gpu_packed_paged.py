@@ -148,3 +148,29 @@ def test_paged_decode_bad_device_arguments_are_reported(kb):
     assert kb.kb_attn_check_device_status(None) == kb.KB_ERR_INVALID_ARG
     kb.decode_paged(qd, kp, vp, table, torch.tensor([256, 1], dtype=torch.int32, device="cuda"))
     assert kb.kb_attn_check_device_status(None) == kb.KB_OK
+
+
+@pytest.mark.parametrize("page_size", [128, 384])
+@pytest.mark.parametrize("start,L", [(0, 1100), (0, 33), (200, 300), (1000, 100), (1099, 1), (64, 32), (500, 17)])
+def test_paged_chunks_bitwise_equal_prefill(kb, seq, page_size, start, L):
+    """Chunks against a shuffled paged pool (unused rows NaN) give the prefill bits."""
+    import torch
+
+    x, q, k, v, pre = seq
+    B = q.shape[0]
+    filled = np.full(B, start + L, dtype=np.int32)
+    kp, vp, table = _paged(k, v, filled, page_size, seed=75_000 + start + L)
+    out = from_dev(kb.chunk_paged(q[:, :, start:start + L].contiguous(), kp, vp, table, start))
+    kb.check_device_status()
+    assert np.array_equal(out, pre[:, :, start:start + L])
+
+
+def test_paged_chunk_bad_page_is_reported(kb):
+    import torch
+
+    x = inputs.make_qkv(1, 256, seed=76_000)
+    q = to_dev(x.q)
+    kp = torch.zeros(2, HKV, 128, D, dtype=torch.bfloat16, device="cuda")
+    table = torch.tensor([[0, 9]], dtype=torch.int32, device="cuda")
+    kb.chunk_paged(q, kp, kp, table, 0)
+    assert kb.kb_attn_check_device_status(None) == kb.KB_ERR_INVALID_ARG
