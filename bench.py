@@ -43,7 +43,7 @@ def workload_name():
             f"Hq={HQ} Hkv={HKV} D={D} bf16")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # ncu dram bytes per launch for the current kernels (profiles/ summaries); None = not captured
-NCU_TRAFFIC_BYTES = {"prefill": None, "decode": 540.3e6}
+NCU_TRAFFIC_BYTES = {"prefill": None, "decode": 537.19e6}
 
 
 def prefill_flops(B: int, S: int) -> int:
@@ -305,49 +305,82 @@ def run_ours(args, rank, world, local):
     emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks, x)
 
 
+def pipelined_e2e(n, host_in, dev_sets, host_out, launch):
+    """Per-step time (ms) of n steps, each copying its inputs from pinned host
+    memory, computing, and copying its result back.  Two device buffer sets
+    and two copy streams let step i+1's upload and step i-1's download run
+    under step i's kernels; every byte of every step still crosses inside the
+    timed region."""
+    import torch
+
+    cs = torch.cuda.current_stream()
+    up = torch.cuda.Stream()
+    down = torch.cuda.Stream()
+    ev_up = [torch.cuda.Event() for _ in range(n)]
+    ev_comp = [torch.cuda.Event() for _ in range(n)]
+    ev_down = [torch.cuda.Event() for _ in range(n)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(up)
+    for i in range(n):
+        s = i % 2
+        ins, out = dev_sets[s]
+        if i >= 2:
+            up.wait_event(ev_comp[i - 2])          # buffer set s is free once step i-2 has computed
+        with torch.cuda.stream(up):
+            for d, h in zip(ins, host_in):
+                d.copy_(h, non_blocking=True)
+        ev_up[i].record(up)
+        cs.wait_event(ev_up[i])
+        if i >= 2:
+            cs.wait_event(ev_down[i - 2])          # ... and its result has been read back
+        launch(ins, out)
+        ev_comp[i].record(cs)
+        down.wait_event(ev_comp[i])
+        with torch.cuda.stream(down):
+            host_out[s].copy_(out, non_blocking=True)
+        ev_down[i].record(down)
+    t1.record(down)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / n
+
+
 def run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_attn):
     import numpy as np
     import torch
 
-    n = args.steps
+    n = max(4, min(args.steps, 12))
     pf = prefill_flops(PREFILL_B, PREFILL_S)
     db = decode_bytes(DECODE_B, DECODE_CTX)
-    hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
-                  for a in (x.q, x.k, x.v))
-    hqd, hkd, hvd = (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
-                     for a in (y.q, y.k, y.v))
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    hod = torch.empty(od.shape, dtype=od.dtype).pin_memory()
-    h2d = sum(t.numel() * 2 for t in (hq, hk, hv, hqd, hkd, hvd))
-    d2h = (ho.numel() + hod.numel()) * 2
-    e2e_n = max(1, min(n, 10))
-    ee = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e2e_n)]
+
+    def pinned(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    hq, hk, hv = pinned(x.q), pinned(x.k), pinned(x.v)
+    hqd, hkd, hvd = pinned(y.q), pinned(y.k), pinned(y.v)
+    ho = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
+    hod = [torch.empty(od.shape, dtype=od.dtype).pin_memory() for _ in range(2)]
+    pre_sets = [([q, k, v], o), ([torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)], torch.empty_like(o))]
+    dec_sets = [([qd, kd, vd], od),
+                ([torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)], torch.empty_like(od))]
     barrier(world, local)
-    torch.cuda.synchronize()
-    for i in range(e2e_n):
-        ee[i][0].record(stream)
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        kb_attn.prefill(q, k, v, out=o)
-        ho.copy_(o, non_blocking=True)
-        ee[i][1].record(stream)
-        qd.copy_(hqd, non_blocking=True)
-        kd.copy_(hkd, non_blocking=True)
-        vd.copy_(hvd, non_blocking=True)
-        kb_attn.decode(qd, kd, vd, DECODE_CTX, out=od)
-        hod.copy_(od, non_blocking=True)
-        ee[i][2].record(stream)
-    torch.cuda.synchronize()
+    pre_ms = pipelined_e2e(n, [hq, hk, hv], pre_sets, ho,
+                           lambda ins, out: kb_attn.prefill(ins[0], ins[1], ins[2], out=out))
+    dec_ms = pipelined_e2e(n, [hqd, hkd, hvd], dec_sets, hod,
+                           lambda ins, out: kb_attn.decode(ins[0], ins[1], ins[2], DECODE_CTX, out=out))
     kb_attn.check_device_status()
-    e2e_pre_ms = reduce_max(statistics.mean(e[0].elapsed_time(e[1]) for e in ee), world,
-                            "cuda" if world > 1 else "cpu")
-    e2e_dec_ms = reduce_max(statistics.mean(e[1].elapsed_time(e[2]) for e in ee), world,
-                            "cuda" if world > 1 else "cpu")
+    # the downloaded results are the kernels' results
+    assert torch.equal(ho[(n - 1) % 2].view(torch.int16), o.view(torch.int16).cpu())
+    e2e_pre_ms = reduce_max(pre_ms, world, "cuda" if world > 1 else "cpu")
+    e2e_dec_ms = reduce_max(dec_ms, world, "cuda" if world > 1 else "cpu")
+    h2d = sum(t.numel() * 2 for t in (hq, hk, hv, hqd, hkd, hvd))
+    d2h = (ho[0].numel() + hod[0].numel()) * 2
     return {"value": aggregate(pf, world, e2e_pre_ms / 1e3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "decode_gbs": aggregate(db, world, e2e_dec_ms / 1e3) / 1e9,
-            "note": "pinned host buffers copied in and results copied out inside every timed step"}
+            "decode_gbs": aggregate(db, world, e2e_dec_ms / 1e3) / 1e9, "steps": n,
+            "note": ("every step uploads its inputs from pinned host memory and downloads its output; "
+                     "two buffer sets let one step's copies overlap the neighbouring step's kernels")}
 
 
 def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks,
