@@ -439,6 +439,64 @@ def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_ma
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args, local):
+    """Time the pages' grid (prefill S x B, decode ctx x B), one JSON line per
+    configuration.  L2 is flushed before every timed launch by reading a 512 MB
+    buffer (a read, so no dirty lines are left for the kernel to write back)."""
+    import torch
+
+    from bitwise_aligned_causal_gb300 import build
+
+    torch.cuda.set_device(local)
+    build.build()
+    from bitwise_aligned_causal_gb300 import kb_attn
+
+    peaks = load_peaks()
+    flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
+    sink = torch.empty(1, dtype=torch.float32, device="cuda")
+    gen = torch.Generator(device="cuda")
+
+    def timed(fn, reps):
+        ts = []
+        for i in range(reps + 3):
+            torch.sum(flush, dim=0, keepdim=True, out=sink)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    for S in (1024, 4096, 8192, 16384):
+        for B in (1, 4, 8, 16):
+            gen.manual_seed(8_000_000 + 100 * (S // 1024) + B)
+            q = torch.randn(B, HQ, S, D, device="cuda", dtype=torch.bfloat16, generator=gen)
+            k = torch.randn(B, HKV, S, D, device="cuda", dtype=torch.bfloat16, generator=gen)
+            v = torch.randn(B, HKV, S, D, device="cuda", dtype=torch.bfloat16, generator=gen)
+            o = torch.empty_like(q)
+            ms = timed(lambda: kb_attn.prefill(q, k, v, out=o), args.steps)
+            tf = prefill_flops(B, S) / (ms / 1e3) / 1e12
+            print(json.dumps({"kind": "prefill", "S": S, "B": B, "ms": ms, "TFLOP/s": tf,
+                              "frac": tf / peaks["bf16_tflops"], "peak_source": peaks["source"]}), flush=True)
+            del q, k, v, o
+    for ctx in (128, 1024, 4096, 8192):
+        for B in (1, 4, 8, 16):
+            gen.manual_seed(9_000_000 + ctx + B)
+            q = torch.randn(B, HQ, 1, D, device="cuda", dtype=torch.bfloat16, generator=gen)
+            k = torch.randn(B, HKV, ctx, D, device="cuda", dtype=torch.bfloat16, generator=gen)
+            v = torch.randn(B, HKV, ctx, D, device="cuda", dtype=torch.bfloat16, generator=gen)
+            o = torch.empty_like(q)
+            ms = timed(lambda: kb_attn.decode(q, k, v, ctx, out=o), args.steps)
+            gbs = decode_bytes(B, ctx) / (ms / 1e3) / 1e9
+            print(json.dumps({"kind": "decode", "ctx": ctx, "B": B, "us": ms * 1e3, "GB/s": gbs,
+                              "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}), flush=True)
+            del q, k, v, o
+    kb_attn.check_device_status()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -449,12 +507,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="full")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every prefill (S x B) and decode (ctx x B) configuration of the grid instead")
     args = ap.parse_args()
     global PREFILL_B, PREFILL_S, DECODE_B, DECODE_CTX
     PREFILL_B, PREFILL_S, DECODE_B, DECODE_CTX = WORKLOADS[args.workload]
     rank, world, local = dist_setup(args.gpus)
     try:
-        if args.impl == "reference":
+        if args.sweep:
+            if rank == 0:
+                run_sweep(args, local)
+        elif args.impl == "reference":
             run_reference(args, rank, world)
         else:
             run_ours(args, rank, world, local)

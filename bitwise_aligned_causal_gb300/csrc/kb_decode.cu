@@ -98,6 +98,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   // Absolute position of query row 0, the sub-chunk's rows [r0, r1) and the
   // key range of the sequence (keys at or beyond seq_kv are never used).
   int pos0 = args.start;
+  int Lb = args.L;                                      // query rows of this sequence (args.L is the row stride)
   if (args.ctx_lens != nullptr) {
     const int ctx = args.ctx_lens[b];
     if (ctx < args.L || ctx > args.max_ctx) {
@@ -106,15 +107,24 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
     pos0 = ctx - args.L;
   }
-  const int seq_kv = pos0 + args.L;
-  const int split = min(args.L, (pos0 / kTileKeys + 1) * kTileKeys - pos0);   // rows before the first tile boundary
+  if (args.starts != nullptr) {
+    pos0 = args.starts[b];
+    Lb = args.lens[b];
+    if (pos0 < 0 || Lb < 0 || Lb > args.L || pos0 + Lb > args.max_ctx) {
+      if (threadIdx.x == 0) atomicCAS(args.err, 0u, static_cast<uint32_t>(kDevBadInput));
+      return;
+    }
+    if (Lb == 0) return;
+  }
+  const int seq_kv = pos0 + Lb;
+  const int split = min(Lb, (pos0 / kTileKeys + 1) * kTileKeys - pos0);   // rows before the first tile boundary
   const int r0 = (sub == 0) ? 0 : split;
-  const int r1 = (sub == 0) ? split : args.L;
+  const int r1 = (sub == 0) ? split : Lb;
   const int Lc = r1 - r0;
   if (Lc <= 0) return;                                  // the chunk does not reach a second tile
   const int n_rows = kGroup * Lc;                       // packed rows in use
   const int n_kv = (pos0 + r1 - 1) / kTileKeys + 1;     // C1: KV tiles 0..floor(last position / 128)
-  const bool zero_tail = (args.block_table != nullptr) || (args.ctx_lens != nullptr);
+  const bool zero_tail = (args.block_table != nullptr) || (args.ctx_lens != nullptr) || (args.starts != nullptr);
   const int tail_from = seq_kv - (n_kv - 1) * kTileKeys;   // first V row of the last tile past the sequence
 
   // Q: packed row m = head i * Lc + rr holds q[b, 4g+i, r0+rr]; unused rows

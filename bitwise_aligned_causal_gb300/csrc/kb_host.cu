@@ -121,8 +121,15 @@ kb_status check_paging(const Paging& pg, int Hkv) {
   return KB_OK;
 }
 
+// Per-sequence start positions and row counts of a ragged batch (device arrays).
+struct Ragged {
+  const int* starts = nullptr;
+  const int* lens = nullptr;
+};
+
 kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int L, int start,
-                     int kv_cap, int q_tiles_per_cta, void* stream, const Paging* paging = nullptr) {
+                     int kv_cap, int q_tiles_per_cta, void* stream, const Paging* paging = nullptr,
+                     const Ragged* ragged = nullptr) {
   kb_status s = check_ptrs(q, k, v, o);
   if (s != KB_OK) return s;
   if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
@@ -131,8 +138,9 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   if (kv_cap > kMaxRows) return KB_ERR_UNSUPPORTED;
   if (q_tiles_per_cta < 0 || q_tiles_per_cta > 2) return KB_ERR_INVALID_ARG;
   if (q_tiles_per_cta == 0 && L > kb::kMaxPackedRows) return KB_ERR_INVALID_ARG;
-  const int first_tile = start / kb::kTileRows;
-  const int last_tile = (start + L - 1) / kb::kTileRows;
+  // a ragged batch sizes the grid for its longest possible sequence
+  const int first_tile = ragged ? 0 : start / kb::kTileRows;
+  const int last_tile = ragged ? (L + kb::kTileRows - 2) / kb::kTileRows : (start + L - 1) / kb::kTileRows;
   // CTAs: tile kernel one per (query tile, batch, head group); packed kernel
   // at most two per (batch, KV head)
   const long long grid = q_tiles_per_cta > 0
@@ -145,10 +153,16 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   for (const void* p : {q, k, v, static_cast<const void*>(o)})
     if ((s = check_device_pointer(p)) != KB_OK) return s;
   if (paging && (s = check_device_pointer(paging->block_table)) != KB_OK) return s;
+  if (ragged) {
+    if ((s = check_device_pointer(ragged->starts)) != KB_OK) return s;
+    if ((s = check_device_pointer(ragged->lens)) != KB_OK) return s;
+  }
 
   CUtensorMap tq, tk, tv;
   const uint64_t row_bytes = kb::kHeadDim * 2u;
-  const uint64_t kv_len = static_cast<uint64_t>(start) + L;
+  // a contiguous uniform batch ends its K/V map at the chunk's last key; a
+  // ragged batch maps the whole cache (the kernels zero V rows past each sequence)
+  const uint64_t kv_len = ragged ? static_cast<uint64_t>(kv_cap) : static_cast<uint64_t>(start) + L;
   // K/V maps: a contiguous cache ends at the chunk's last key (later rows read
   // as zeros); a paged pool is [num_pages * Hkv planes, page_size rows].
   const uint64_t kv_rows = paging ? static_cast<uint64_t>(paging->page_size) : kv_len;
@@ -169,6 +183,10 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
     a.L = L;
     a.start = start;
     a.max_ctx = kv_cap;
+    if (ragged) {
+      a.starts = ragged->starts;
+      a.lens = ragged->lens;
+    }
     if (paging) {
       a.block_table = paging->block_table;
       a.pages_per_seq = paging->pages_per_seq;
@@ -177,7 +195,8 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
     }
     a.err = dst->err;
     const int split = std::min(L, kb::kTileKeys - start % kb::kTileKeys);
-    const cudaError_t e = kb::launch_packed(tk, tv, a, split < L ? 2 : 1, static_cast<cudaStream_t>(stream));
+    const int n_sub = (ragged || split < L) ? 2 : 1;
+    const cudaError_t e = kb::launch_packed(tk, tv, a, n_sub, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return KB_OK;
   }
@@ -194,6 +213,11 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   a.start = start;
   a.first_tile = first_tile;
   a.n_tiles = last_tile - first_tile + 1;
+  a.kv_cap = kv_cap;
+  if (ragged) {
+    a.starts = ragged->starts;
+    a.lens = ragged->lens;
+  }
   if (paging) {
     a.block_table = paging->block_table;
     a.pages_per_seq = paging->pages_per_seq;
@@ -245,6 +269,31 @@ kb_status kb_attn_chunk_paged(const void* q, const void* k_pages, const void* v_
   const long long cap = static_cast<long long>(pages_per_seq) * page_size;
   return chunk_impl(q, k_pages, v_pages, o, B, Hq, Hkv, L, start, static_cast<int>(cap), chunk_cta_shape(L), stream,
                     &pg);
+}
+
+kb_status kb_attn_chunk_varlen(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                               int L_max, const int* starts, const int* lens, int kv_cap, const int* block_table,
+                               int pages_per_seq, int page_size, int num_pages, void* stream) {
+  kb_status s = check_heads(B, Hq, Hkv);
+  if (s != KB_OK) return s;
+  if (!starts || !lens || (reinterpret_cast<uintptr_t>(starts) & 3u) || (reinterpret_cast<uintptr_t>(lens) & 3u))
+    return KB_ERR_INVALID_ARG;
+  Ragged rg;
+  rg.starts = starts;
+  rg.lens = lens;
+  if (block_table) {
+    Paging pg;
+    pg.block_table = block_table;
+    pg.pages_per_seq = pages_per_seq;
+    pg.page_size = page_size;
+    pg.num_pages = num_pages;
+    if ((s = check_paging(pg, Hkv)) != KB_OK) return s;
+    const int cap = pages_per_seq * page_size;
+    if (L_max < 1 || L_max > cap) return KB_ERR_INVALID_ARG;
+    return chunk_impl(q, k, v, o, B, Hq, Hkv, L_max, 0, cap, chunk_cta_shape(L_max), stream, &pg, &rg);
+  }
+  if (L_max < 1 || kv_cap < 1 || L_max > kv_cap) return KB_ERR_INVALID_ARG;
+  return chunk_impl(q, k, v, o, B, Hq, Hkv, L_max, 0, kv_cap, chunk_cta_shape(L_max), stream, nullptr, &rg);
 }
 
 kb_status kb_attn_decode(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int ctx_len,

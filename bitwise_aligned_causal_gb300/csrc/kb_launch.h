@@ -17,6 +17,9 @@ struct PrefillArgs {
   int n_tiles;      // absolute query tiles touched by [start, start+L)
   const int* block_table;  // optional device [B, pages_per_seq]: paged K/V pools
   int pages_per_seq, page_size, num_pages;
+  const int* starts;       // optional device [B]: per-sequence start (ragged batch; then
+  const int* lens;         //   L is the row stride of q and o and lens[b] <= L rows are used)
+  int kv_cap;              // keys per sequence the cache can hold
   uint32_t* err;    // device error word
 };
 
@@ -31,6 +34,8 @@ struct PackedArgs {
   int max_ctx;             // largest valid ctx_lens entry (cache capacity)
   const int* block_table;  // optional device [B, pages_per_seq]: paged K/V pools
   int pages_per_seq, page_size, num_pages;
+  const int* starts;       // optional device [B]: per-sequence start and row count (ragged
+  const int* lens;         //   batch); L is then the row stride of q and o
   uint32_t* err;
 };
 

@@ -83,7 +83,22 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
   const int b = rem / units_per_bt;
   const int h0 = (rem % units_per_bt) * NQ;
   const int g = h0 / kGroup;
-  const int t = args.first_tile + args.n_tiles - 1 - tile_rank;   // absolute query tile
+  // this sequence's query rows: positions start .. start+L-1 (per sequence
+  // in a ragged batch, where L is only the row stride of q and o)
+  int start = args.start, L = args.L, first_tile = args.first_tile, n_tiles = args.n_tiles;
+  if (args.starts != nullptr) {
+    start = args.starts[b];
+    L = args.lens[b];
+    if (start < 0 || L < 0 || L > args.L || start + L > args.kv_cap) {
+      if (threadIdx.x == 0) atomicCAS(args.err, 0u, static_cast<uint32_t>(kDevBadInput));
+      return;
+    }
+    if (L == 0) return;
+    first_tile = start / kTileRows;
+    n_tiles = (start + L - 1) / kTileRows - first_tile + 1;
+  }
+  if (tile_rank >= n_tiles) return;                                // grid sized for the longest sequence
+  const int t = first_tile + n_tiles - 1 - tile_rank;              // absolute query tile
   const int n_kv = t + 1;                                          // C1: KV tiles 0..t
 
   if (threadIdx.x == 0) {
@@ -107,7 +122,10 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
   const bool skip = (*abort_flag != 0);
 
   const bool paged = args.block_table != nullptr;
-  const int kv_len = args.start + args.L;                          // keys at or beyond kv_len are never used
+  const int kv_len = start + L;                                    // keys at or beyond kv_len are never used
+  // the K/V map ends at kv_len only for a contiguous, uniform batch; else the
+  // last tile's V rows past kv_len are zeroed in shared memory
+  const bool zero_tail = paged || (args.starts != nullptr);
   if (warp == Cfg::kLoadWarp) {
     // ------------------------------------------------------------ producer
     if (!skip) {
@@ -116,7 +134,7 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
-        const int yq = t * kTileRows - args.start;      // may be negative: zero-filled rows
+        const int yq = t * kTileRows - start;           // may be negative: zero-filled rows
         mbar_arrive_expect_tx(bar(Cfg::kBarQFull), NQ * kTileBytes);
         for (int qi = 0; qi < NQ; ++qi) {
           const int zq = b * args.Hq + h0 + qi;
@@ -164,9 +182,10 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
         }
         issued = 2 * j + 2;
       }
-      if (ok && paged) {
-        // V rows past kv_len in the last tile belong to the page's unused
-        // part and may hold anything (NaN): zero them so P = 0 adds nothing.
+      if (ok && zero_tail) {
+        // V rows past kv_len in the last tile may hold anything (a page's
+        // unused part, another position's data, NaN): zero them so P = 0 adds
+        // nothing.
         const int jl = n_kv - 1;
         const int slot = jl % Cfg::kStages;
         ok = mbar_wait(bar(Cfg::kBarVFull + slot), (jl / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
@@ -217,7 +236,7 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
       for (int j = 0; j < n_kv && ok; ++j) {
         const int slot = j % Cfg::kStages;
         const int nslot = (j + 1) % Cfg::kStages;
-        if (paged && j == n_kv - 1)
+        if (zero_tail && j == n_kv - 1)
           ok = mbar_wait(bar(Cfg::kBarVReady), 0, abort_flag, args.err, kDevTimeoutTma);
         else
           ok = mbar_wait(bar(Cfg::kBarVFull + slot), (j / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
@@ -298,8 +317,8 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
     if (ok) {
       tc_fence_after();
       const int pos = t * kTileRows + r;
-      const int i = pos - args.start;
-      const bool store = (i >= 0) && (i < args.L);
+      const int i = pos - start;
+      const bool store = (i >= 0) && (i < L);
       const float inv_l = row_inv_l(st);
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.o) +
                                             ((static_cast<size_t>(b) * args.Hq + h0 + qi) * args.L + (store ? i : 0)) *

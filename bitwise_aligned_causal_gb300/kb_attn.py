@@ -35,6 +35,7 @@ _SIGS = {
     "kb_attn_decode": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
     "kb_attn_decode_paged": [_P, _P, _P, _P, _I, _I, _I, _P, _I, _I, _I, _P, _P],
     "kb_attn_chunk_paged": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _I, _I, _P],
+    "kb_attn_chunk_varlen": [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _P, _I, _I, _I, _P],
     "kb_attn_check_device_status": [_P],
     "kb_attn_debug_wait_timeout": [_I, _P],
     "kb_attn_chunk_cta_shape": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P],
@@ -100,6 +101,12 @@ def kb_attn_chunk_paged(q, k_pages, v_pages, o, B, Hq, Hkv, L, start, block_tabl
                         num_pages, stream=None) -> int:
     return _lib.kb_attn_chunk_paged(q, k_pages, v_pages, o, B, Hq, Hkv, L, start, block_table, pages_per_seq,
                                     page_size, num_pages, stream)
+
+
+def kb_attn_chunk_varlen(q, k, v, o, B, Hq, Hkv, L_max, starts, lens, kv_cap, block_table, pages_per_seq,
+                         page_size, num_pages, stream=None) -> int:
+    return _lib.kb_attn_chunk_varlen(q, k, v, o, B, Hq, Hkv, L_max, starts, lens, kv_cap, block_table, pages_per_seq,
+                                     page_size, num_pages, stream)
 
 
 def kb_attn_chunk_cta_shape(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, q_tiles_per_cta, stream=None) -> int:
@@ -223,6 +230,32 @@ def chunk_paged(q, k_pages, v_pages, block_table, start, out=None, stream=None):
     _raise(kb_attn_chunk_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), o.data_ptr(), B, Hq, Hkv, L,
                                int(start), block_table.data_ptr(), block_table.shape[1], page_size, num_pages,
                                _stream(stream)), "kb_attn_chunk_paged")
+    return o
+
+
+def chunk_varlen(q, k, v, starts, lens, out=None, block_table=None, stream=None):
+    """Ragged batch: q [B,Hq,L_max,128]; per-sequence starts/lens int32 [B] on the device; k/v either
+    contiguous caches [B,Hkv,cap,128] or, with block_table [B,pages_per_seq], pools [num_pages,Hkv,page,128]."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, 4)
+    for t, n in ((starts, "starts"), (lens, "lens")) + (((block_table, "block_table"),) if block_table is not None
+                                                         else ()):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+            raise TypeError(f"{n} must be a contiguous int32 CUDA tensor")
+    B, Hq, L_max = q.shape[0], q.shape[1], q.shape[2]
+    o = torch.empty_like(q) if out is None else out
+    _check(o, "out", 4)
+    if block_table is None:
+        Hkv, cap = k.shape[1], k.shape[2]
+        st = kb_attn_chunk_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, L_max,
+                                  starts.data_ptr(), lens.data_ptr(), cap, None, 0, 0, 0, _stream(stream))
+    else:
+        num_pages, Hkv, page_size = k.shape[0], k.shape[1], k.shape[2]
+        st = kb_attn_chunk_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, L_max,
+                                  starts.data_ptr(), lens.data_ptr(), 0, block_table.data_ptr(),
+                                  block_table.shape[1], page_size, num_pages, _stream(stream))
+    _raise(st, "kb_attn_chunk_varlen")
     return o
 
 

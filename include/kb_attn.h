@@ -96,6 +96,31 @@ kb_status kb_attn_chunk_paged(const void* q, const void* k_pages, const void* v_
                               int pages_per_seq, int page_size, int num_pages, void* stream);
 
 /*
+ * Ragged batch: chunked forward where every sequence has its own start
+ * position and row count (device int32 arrays), against a contiguous cache
+ * (block_table == NULL) or a paged pool.  A full prefill of sequences of
+ * different lengths is starts[b] = 0, lens[b] = S_b.  (The per-sequence
+ * lengths are this library's addition; the pages' workloads are uniform.)
+ *   q, o     : [B, Hq, L_max, 128]; row i < lens[b] of batch b is position
+ *              starts[b] + i; rows lens[b]..L_max-1 are neither read for any
+ *              other row nor written
+ *   k, v     : block_table == NULL: [B, Hkv, kv_cap, 128]
+ *              else pools [num_pages, Hkv, page_size, 128] addressed as in
+ *              kb_attn_chunk_paged (kv_cap is then pages_per_seq * page_size)
+ *   starts,
+ *   lens     : device int32 [B]; 0 <= lens[b] <= L_max, starts[b] >= 0,
+ *              starts[b] + lens[b] <= kv_cap; keys 0..starts[b]+lens[b]-1 of
+ *              every sequence must be written, later cache rows may hold anything
+ * Bits equal kb_attn_chunk on each sequence alone.  Out-of-range starts, lens
+ * or page indices are found on the device: those sequences are not written and
+ * the next kb_attn_check_device_status returns KB_ERR_INVALID_ARG.
+ */
+kb_status kb_attn_chunk_varlen(const void* q, const void* k, const void* v, void* o,
+                               int B, int Hq, int Hkv, int L_max, const int* starts, const int* lens,
+                               int kv_cap, const int* block_table, int pages_per_seq, int page_size,
+                               int num_pages, void* stream);
+
+/*
  * One-token decode over a paged KV cache, one context length per sequence
  * (README "Usage": unified_decode; the page table is this library's
  * addition, the pages show only a contiguous cache).

@@ -111,3 +111,12 @@ def test_packed_path_host_checks_do_not_trap(kb):
     assert st in (kb.KB_ERR_CUDA, kb.KB_ERR_INVALID_ARG)
     st = kb.kb_attn_chunk(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 16, 0, 64)
     assert st in (kb.KB_ERR_CUDA, kb.KB_ERR_INVALID_ARG)
+
+
+def test_varlen_arguments_rejected(kb):
+    args = (FAKE, FAKE, FAKE, FAKE, 2, 32, 8)
+    assert kb.kb_attn_chunk_varlen(*args, 16, None, FAKE, 64, None, 0, 0, 0) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_chunk_varlen(*args, 16, FAKE, FAKE + 2, 64, None, 0, 0, 0) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_chunk_varlen(*args, 0, FAKE, FAKE, 64, None, 0, 0, 0) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_chunk_varlen(*args, 65, FAKE, FAKE, 64, None, 0, 0, 0) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_chunk_varlen(*args, 16, FAKE, FAKE, 0, FAKE, 2, 192, 4) == kb.KB_ERR_UNSUPPORTED
