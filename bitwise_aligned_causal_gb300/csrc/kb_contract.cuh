@@ -177,6 +177,57 @@ __device__ __forceinline__ float row_softmax_tile(const uint32_t (&s)[128], int 
   return alpha;
 }
 
+// The same tile step with a row spread over four threads (a quad of lanes
+// 4i..4i+3, thread u = lane % 4), as the 16x256b TMEM load lays it out:
+// thread u holds keys 8r+2u and 8r+2u+1 (x[2r], x[2r+1]) for r = 0..15, which
+// are exactly the keys of the partial sums k mod 8 = 2u and 2u+1 above.  The
+// max and the pair sums are combined across the quad with shuffles in the
+// same order as the single-thread tree, so the bits are the same; p[r] is the
+// bf16 pair of keys 8r+2u, 8r+2u+1 (TMEM column 4r+u of P).  All 32 lanes of
+// the warp must call it together.
+template <bool kMasked>
+__device__ __forceinline__ float row_softmax_tile_quad(float (&x)[32], int u, int n_valid, RowState& st,
+                                                       uint32_t (&p)[16]) {
+  const float c = score_scale_log2();
+  if (kMasked) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      x[2 * r] = (8 * r + 2 * u < n_valid) ? x[2 * r] : -INFINITY;
+      x[2 * r + 1] = (8 * r + 2 * u + 1 < n_valid) ? x[2 * r + 1] : -INFINITY;
+    }
+  }
+  float mx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mx[i] = max3(x[i], x[i + 8], fmaxf(x[i + 16], x[i + 24]));
+  float tile_max = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+  tile_max = fmaxf(tile_max, __shfl_xor_sync(0xffffffffu, tile_max, 1));
+  tile_max = fmaxf(tile_max, __shfl_xor_sync(0xffffffffu, tile_max, 2));
+
+  float alpha = 1.0f;
+  if (__fsub_rn(tile_max, st.m) > kRescaleThresholdRaw) {
+    const float mc_new = __fmul_rn(tile_max, c);
+    alpha = ex2_approx(__fmaf_rn(st.m, c, -mc_new));
+    st.m = tile_max;
+    st.mc = mc_new;
+  }
+  const float2 c2 = make_float2(c, c);
+  const float2 nmc2 = make_float2(-st.mc, -st.mc);
+  float2 acc;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const float2 arg = __ffma2_rn(make_float2(x[2 * r], x[2 * r + 1]), c2, nmc2);
+    const float w0 = ex2_approx(arg.x);
+    const float w1 = ex2_approx(arg.y);
+    acc = (r == 0) ? make_float2(w0, w1) : __fadd2_rn(acc, make_float2(w0, w1));
+    p[r] = pack_bf16x2(w0, w1);
+  }
+  const float s_pair = __fadd_rn(acc.x, acc.y);                                      // acc[u].x + acc[u].y
+  const float s_half = __fadd_rn(s_pair, __shfl_xor_sync(0xffffffffu, s_pair, 1)); // (0+1) or (2+3)
+  const float tile_sum = __fadd_rn(s_half, __shfl_xor_sync(0xffffffffu, s_half, 2));
+  st.l = __fmaf_rn(st.l, alpha, tile_sum);
+  return alpha;
+}
+
 // Scale 32 accumulator columns by alpha (bit-neutral when alpha == 1).
 __device__ __forceinline__ void rescale32(uint32_t (&o)[32], float alpha) {
   const float2 a2 = make_float2(alpha, alpha);

@@ -10,8 +10,9 @@
 // tcgen05.mma shape, k-order and row softmax as prefill and every packed row
 // reproduces the prefill row exactly, while K and V are read once per KV head.
 // A sub-chunk never crosses a 128-position tile boundary, so all its rows end
-// on the same KV tile.  K/V tiles stream through a three-deep TMA ring; S is
-// double-buffered in TMEM so the next Q K^T overlaps the current softmax.
+// on the same KV tile.  K/V tiles stream through a three-deep TMA ring; S has
+// three TMEM buffers, so the next two Q K^T products run ahead of the softmax
+// (P of a tile lives in its S buffer until that tile's P V has finished).
 //   warps 0..NS-1  softmax (TMEM lanes 32w..32w+31; NS = 1 narrow, 4 wide)
 //   warp  NS       TMA producer (lane 0 issues; the warp zeroes a V tail)
 //   warp  NS+1     TMEM allocator + MMA issuer (one lane)
@@ -30,7 +31,9 @@ struct PackedCfg {
   static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
   static constexpr int kStages = 3;
   static constexpr int kQRows = kWide ? 128 : 8;
-  static constexpr uint32_t kTmemCols = 512;                  // S0, S1, O (128 columns each)
+  static constexpr int kSBufs = 3;
+  static constexpr uint32_t kTmemCols = 512;                  // S0, S1, S2, O (128 columns each)
+  static constexpr uint32_t kOCol = kSBufs * 128u;
   static constexpr uint32_t kQSlab = kQRows * 128;            // bytes of one 64-column slab of Q
   static constexpr uint32_t kQSbo = kWide ? 1024u : 0u;
   static constexpr uint32_t kQOff = 0;
@@ -41,10 +44,10 @@ struct PackedCfg {
   static constexpr int kBarKEmpty = kBarKFull + kStages;
   static constexpr int kBarVFull = kBarKEmpty + kStages;
   static constexpr int kBarVEmpty = kBarVFull + kStages;
-  static constexpr int kBarSFull = kBarVEmpty + kStages;   // 2 (double-buffered S)
-  static constexpr int kBarPFull = kBarSFull + 2;
-  static constexpr int kBarOFull = kBarPFull + 1;
-  static constexpr int kBarVReady = kBarOFull + 1;         // last V tile with its tail zeroed
+  static constexpr int kBarSFull = kBarVEmpty + kStages;   // one per S buffer
+  static constexpr int kBarPFull = kBarSFull + kSBufs;
+  static constexpr int kBarOFull = kBarPFull + 1;          // one per S buffer: P V of a tile using it done
+  static constexpr int kBarVReady = kBarOFull + kSBufs;    // last V tile with its tail zeroed
   static constexpr int kBarDrain = kBarVReady + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
@@ -184,8 +187,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if (lane == 0) {
           const uint32_t kdst = sbase + Cfg::kKOff + slot * kTileBytes;
           mbar_arrive_expect_tx(bar(Cfg::kBarKFull + slot), kTileBytes);
-          tma_load_3d_hint(kdst, &tmap_k, 0, row, plane, bar(Cfg::kBarKFull + slot), stream_once);
-          tma_load_3d_hint(kdst + kSlabBytes, &tmap_k, 64, row, plane, bar(Cfg::kBarKFull + slot), stream_once);
+          tma_load_tile_hint(kdst, &tmap_k, row, plane, bar(Cfg::kBarKFull + slot), stream_once);
         }
         issued = 2 * j + 1;
         if (j >= Cfg::kStages)
@@ -195,8 +197,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if (lane == 0) {
           const uint32_t vdst = sbase + Cfg::kVOff + slot * kTileBytes;
           mbar_arrive_expect_tx(bar(Cfg::kBarVFull + slot), kTileBytes);
-          tma_load_3d_hint(vdst, &tmap_v, 0, row, plane, bar(Cfg::kBarVFull + slot), stream_once);
-          tma_load_3d_hint(vdst + kSlabBytes, &tmap_v, 64, row, plane, bar(Cfg::kBarVFull + slot), stream_once);
+          tma_load_tile_hint(vdst, &tmap_v, row, plane, bar(Cfg::kBarVFull + slot), stream_once);
         }
         issued = 2 * j + 2;
       }
@@ -244,13 +245,15 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           const int jn = j + 1;
           const int slot = jn % Cfg::kStages;
           ok = mbar_wait(bar(Cfg::kBarKFull + slot), (jn / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
-          // S buffer jn%2 held P of tile j-1: free once that P V has finished
-          if (ok && jn >= 2) ok = mbar_wait(bar(Cfg::kBarOFull), (j - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
+          // S buffer jn%3 held P of tile jn-3: free once that P V has finished
+          const int sb = jn % Cfg::kSBufs;
+          if (ok && jn >= Cfg::kSBufs)
+            ok = mbar_wait(bar(Cfg::kBarOFull + sb), ((jn - Cfg::kSBufs) / Cfg::kSBufs) & 1, abort_flag, args.err,
+                           kDevTimeoutMma);
           if (!ok) break;
           tc_fence_after();
-          issue_qk(tmem_base + (jn & 1) * 128u, q_saddr, Cfg::kQSbo, Cfg::kQSlab,
-                   sbase + Cfg::kKOff + slot * kTileBytes);
-          tc_commit(bar(Cfg::kBarSFull + (jn & 1)));
+          issue_qk(tmem_base + sb * 128u, q_saddr, Cfg::kQSbo, Cfg::kQSlab, sbase + Cfg::kKOff + slot * kTileBytes);
+          tc_commit(bar(Cfg::kBarSFull + sb));
           tc_commit(bar(Cfg::kBarKEmpty + slot));
         }
         const int slot = j % Cfg::kStages;
@@ -264,8 +267,9 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         if (!ok) break;
         tc_fence_after();
-        issue_pv(tmem_base + 256u, tmem_base + (j & 1) * 128u, sbase + Cfg::kVOff + slot * kTileBytes, j == 0);
-        tc_commit(bar(Cfg::kBarOFull));
+        issue_pv(tmem_base + Cfg::kOCol, tmem_base + (j % Cfg::kSBufs) * 128u, sbase + Cfg::kVOff + slot * kTileBytes,
+                 j == 0);
+        tc_commit(bar(Cfg::kBarOFull + j % Cfg::kSBufs));
         tc_commit(bar(Cfg::kBarVEmpty + slot));
       }
       if (!ok) {
@@ -273,40 +277,45 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         packed_drain_wait(bar(Cfg::kBarDrain), 0);
       }
     }
-  } else {
-    // ------------------------------------------------------------- softmax
+  } else if (kWide) {
+    // ------------------------------------------------- softmax, row per thread
     const int m = warp * 32 + lane;                    // packed row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t o_tmem = tmem_base + 256u + lane_off;
+    const uint32_t o_tmem = tmem_base + Cfg::kOCol + lane_off;
     const int head = (m < n_rows) ? m / Lc : 0;
     const int r = (m < n_rows) ? r0 + m % Lc : r0;     // unused rows take the sub-chunk's first position
     const int pos = pos0 + r;
     RowState st = row_state_init();
     bool ok = !skip;
     for (int j = 0; j < n_kv && ok; ++j) {
-      ok = mbar_wait(bar(Cfg::kBarSFull + (j & 1)), (j >> 1) & 1, abort_flag, args.err, kDevTimeoutMma);
+      ok = mbar_wait(bar(Cfg::kBarSFull + j % Cfg::kSBufs), (j / Cfg::kSBufs) & 1, abort_flag, args.err,
+                     kDevTimeoutMma);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t s_tmem = tmem_base + (j & 1) * 128u + lane_off;
+      const uint32_t s_tmem = tmem_base + (j % Cfg::kSBufs) * 128u + lane_off;
       uint32_t s[128];
       tmem_ld128_wait(s_tmem, s);
       uint32_t p[64];
       const float alpha = (j == n_kv - 1) ? row_softmax_tile<true>(s, pos - j * kTileKeys + 1, st, p)
                                           : row_softmax_tile<false>(s, kTileKeys, st, p);
-      if (j > 0) {
-        ok = mbar_wait(bar(Cfg::kBarOFull), (j - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
+      // O is rescaled only when some row's reference max moved, and only then
+      // must the previous tile's P V have finished (its barrier is that tile's
+      // S buffer's; the MMA issuer's wait before reusing an S buffer keeps it
+      // at most one phase away).  P of this tile goes to its own S buffer, so
+      // publishing it needs no wait.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        ok = mbar_wait(bar(Cfg::kBarOFull + (j - 1) % Cfg::kSBufs), ((j - 1) / Cfg::kSBufs) & 1, abort_flag,
+                       args.err, kDevTimeoutMma);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32_wait(o_tmem + c * 32u, o);
-            rescale32(o, alpha);
-            tmem_st32(o_tmem + c * 32u, o);
-          }
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32_wait(o_tmem + c * 32u, o);
+          rescale32(o, alpha);
+          tmem_st32(o_tmem + c * 32u, o);
         }
       }
       {
@@ -320,7 +329,9 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       tc_fence_before();
       mbar_arrive(bar(Cfg::kBarPFull));
     }
-    if (ok) ok = mbar_wait(bar(Cfg::kBarOFull), (n_kv - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
+    if (ok)
+      ok = mbar_wait(bar(Cfg::kBarOFull + (n_kv - 1) % Cfg::kSBufs), ((n_kv - 1) / Cfg::kSBufs) & 1, abort_flag,
+                     args.err, kDevTimeoutMma);
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after();
@@ -329,6 +340,97 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       uint4* dst = reinterpret_cast<uint4*>(
           static_cast<__nv_bfloat16*>(args.o) +
           ((static_cast<size_t>(b) * args.Hq + g * kGroup + head) * args.L + r) * kHeadDim);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32], w[16];
+        tmem_ld32_wait(o_tmem + c * 32u, o);
+        normalise32(o, inv_l, w);
+        if (store) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[c * 4 + v4] = make_uint4(w[4 * v4 + 0], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------- softmax, four threads per row (narrow)
+    // Rows 0..7 live in TMEM lanes 0..7; the 16x256b load gives each quad of
+    // lanes 4i..4i+3 row i, thread u holding keys 8r+2u, 8r+2u+1 (r = 0..15),
+    // so the row's 128 exponentials are spread over four threads.
+    const int m = lane >> 2;                           // packed row 0..7
+    const int u = lane & 3;
+    const uint32_t o_tmem = tmem_base + Cfg::kOCol;    // warp 0: lanes 0..31
+    const int head = (m < n_rows) ? m / Lc : 0;
+    const int r = (m < n_rows) ? r0 + m % Lc : r0;     // unused rows take the sub-chunk's first position
+    const int pos = pos0 + r;
+    RowState st = row_state_init();
+    bool ok = !skip;
+    for (int j = 0; j < n_kv && ok; ++j) {
+      ok = mbar_wait(bar(Cfg::kBarSFull + j % Cfg::kSBufs), (j / Cfg::kSBufs) & 1, abort_flag, args.err,
+                     kDevTimeoutMma);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t s_tmem = tmem_base + (j % Cfg::kSBufs) * 128u;
+      float x[32];
+      {
+        uint32_t v[32];
+        tmem_ld_16x256b_x8_wait(s_tmem, v);            // keys 0..63
+#pragma unroll
+        for (int q = 0; q < 8; ++q) { x[2 * q] = __uint_as_float(v[4 * q]); x[2 * q + 1] = __uint_as_float(v[4 * q + 1]); }
+        tmem_ld_16x256b_x8_wait(s_tmem + 64u, v);      // keys 64..127
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          x[16 + 2 * q] = __uint_as_float(v[4 * q]);
+          x[16 + 2 * q + 1] = __uint_as_float(v[4 * q + 1]);
+        }
+      }
+      uint32_t p[16];
+      const float alpha = (j == n_kv - 1) ? row_softmax_tile_quad<true>(x, u, pos - j * kTileKeys + 1, st, p)
+                                          : row_softmax_tile_quad<false>(x, u, kTileKeys, st, p);
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        // rescale O (rows in lanes 0..31 through the 32x32b shape; lane L takes
+        // the factor of row L % 8, rows 8..31 are never stored)
+        ok = mbar_wait(bar(Cfg::kBarOFull + (j - 1) % Cfg::kSBufs), ((j - 1) / Cfg::kSBufs) & 1, abort_flag,
+                       args.err, kDevTimeoutMma);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const float a_lane = __shfl_sync(0xffffffffu, alpha, 4 * (lane & 7));
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32_wait(o_tmem + c * 32u, o);
+          rescale32(o, a_lane);
+          tmem_st32(o_tmem + c * 32u, o);
+        }
+      }
+      {
+        uint32_t pv[32];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) { pv[2 * q] = p[q]; pv[2 * q + 1] = p[q]; }   // lanes m and m + 8
+        tmem_st_16x128b_x16(s_tmem, pv);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(Cfg::kBarPFull));
+    }
+    if (ok)
+      ok = mbar_wait(bar(Cfg::kBarOFull + (n_kv - 1) % Cfg::kSBufs), ((n_kv - 1) / Cfg::kSBufs) & 1, abort_flag,
+                     args.err, kDevTimeoutMma);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      // lane L < 8 stores row L; its l comes from the quad that owns the row
+      const float l_lane = __shfl_sync(0xffffffffu, st.l, 4 * (lane & 7));
+      const float inv_l = __frcp_rn(l_lane);
+      const int row = lane;
+      const bool store = row < n_rows;
+      const int s_head = store ? row / Lc : 0;
+      const int s_r = store ? r0 + row % Lc : r0;
+      uint4* dst = reinterpret_cast<uint4*>(
+          static_cast<__nv_bfloat16*>(args.o) +
+          ((static_cast<size_t>(b) * args.Hq + g * kGroup + s_head) * args.L + s_r) * kHeadDim);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32], w[16];

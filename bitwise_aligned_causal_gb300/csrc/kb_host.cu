@@ -79,15 +79,18 @@ kb_status check_device_pointer(const void* p) {
   return KB_OK;
 }
 
-// Rows of 128 bf16, box of 64 columns x 128 rows, 128-byte swizzle.
-// `rows` rows are in bounds in each of `planes` planes `plane_stride` bytes
-// apart; reads beyond `rows` are zero-filled by the TMA unit.
+// Rows of 128 bf16 seen as a 4-D tensor (64 columns, rows, 2 column halves,
+// planes): the halves are 128 bytes apart inside a row, so one box of
+// {64, 128, 2} moves a whole 128-row tile into the two 128-byte-swizzled
+// slabs the MMA descriptors expect.  `rows` rows are in bounds in each of
+// `planes` planes `plane_stride` bytes apart; reads beyond `rows` are
+// zero-filled by the TMA unit.
 kb_status encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes, uint64_t plane_stride) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kb::kHeadDim), rows, planes};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kb::kHeadDim) * 2u, plane_stride};
-  cuuint32_t box[3] = {64u, 128u, 1u};
-  cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  cuuint64_t dims[4] = {64u, rows, 2u, planes};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kb::kHeadDim) * 2u, 128u, plane_stride};
+  cuuint32_t box[4] = {64u, 128u, 2u, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? KB_OK : KB_ERR_CUDA;

@@ -139,8 +139,7 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
         for (int qi = 0; qi < NQ; ++qi) {
           const int zq = b * args.Hq + h0 + qi;
           const uint32_t dst = sbase + Cfg::kQOff + qi * kTileBytes;
-          tma_load_3d(dst, &tmap_q, 0, yq, zq, bar(Cfg::kBarQFull));
-          tma_load_3d(dst + kSlabBytes, &tmap_q, 64, yq, zq, bar(Cfg::kBarQFull));
+          tma_load_tile(dst, &tmap_q, yq, zq, bar(Cfg::kBarQFull));
         }
       }
       int issued = 0;
@@ -166,8 +165,7 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
         if (lane == 0) {
           const uint32_t kdst = sbase + Cfg::kKOff + slot * kTileBytes;
           mbar_arrive_expect_tx(bar(Cfg::kBarKFull + slot), kTileBytes);
-          tma_load_3d_hint(kdst, &tmap_k, 0, row, plane, bar(Cfg::kBarKFull + slot), keep);
-          tma_load_3d_hint(kdst + kSlabBytes, &tmap_k, 64, row, plane, bar(Cfg::kBarKFull + slot), keep);
+          tma_load_tile_hint(kdst, &tmap_k, row, plane, bar(Cfg::kBarKFull + slot), keep);
         }
         issued = 2 * j + 1;
         if (j >= Cfg::kStages)
@@ -177,8 +175,7 @@ kb_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_const
         if (lane == 0) {
           const uint32_t vdst = sbase + Cfg::kVOff + slot * kTileBytes;
           mbar_arrive_expect_tx(bar(Cfg::kBarVFull + slot), kTileBytes);
-          tma_load_3d_hint(vdst, &tmap_v, 0, row, plane, bar(Cfg::kBarVFull + slot), keep);
-          tma_load_3d_hint(vdst + kSlabBytes, &tmap_v, 64, row, plane, bar(Cfg::kBarVFull + slot), keep);
+          tma_load_tile_hint(vdst, &tmap_v, row, plane, bar(Cfg::kBarVFull + slot), keep);
         }
         issued = 2 * j + 2;
       }

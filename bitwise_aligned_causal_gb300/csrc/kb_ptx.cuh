@@ -122,6 +122,27 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// One whole 128-row tile (both 64-column halves) through the 4-D view
+// (64 columns, rows, 2 halves, planes) of a [planes, rows, 128] bf16 tensor:
+// the box {64, 128, 2} lands as the two 16 KB swizzled slabs, half 0 first.
+__device__ __forceinline__ void tma_load_tile(uint32_t dst, const void* tmap, int row, int plane, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(row), "r"(0), "r"(plane), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_tile_hint(uint32_t dst, const void* tmap, int row, int plane, uint32_t bar,
+                                                   uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(row), "r"(0), "r"(plane), "r"(bar),
+        "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -294,6 +315,37 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+
+// 16x256b shape, 8 repetitions: thread t reads lanes base + t/4 and
+// base + t/4 + 8, columns 8r + 2(t%4) and 8r + 2(t%4) + 1 of repetition r;
+// registers 4r, 4r+1 hold the first lane, 4r+2, 4r+3 the second.
+#define KB_R8(b) "=r"(r[b + 0]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), \
+                 "=r"(r[b + 4]), "=r"(r[b + 5]), "=r"(r[b + 6]), "=r"(r[b + 7])
+__device__ __forceinline__ void tmem_ld_16x256b_x8_wait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : KB_R8(0), KB_R8(8), KB_R8(16), KB_R8(24)
+      : "r"(taddr)
+      : "memory");
+}
+#undef KB_R8
+
+// 16x128b shape, 16 repetitions: thread t writes lanes base + t/4 (register
+// 2r) and base + t/4 + 8 (register 2r+1), column 4r + t%4 of repetition r.
+#define KB_V8(b) "r"(v[b + 0]), "r"(v[b + 1]), "r"(v[b + 2]), "r"(v[b + 3]), \
+                 "r"(v[b + 4]), "r"(v[b + 5]), "r"(v[b + 6]), "r"(v[b + 7])
+__device__ __forceinline__ void tmem_st_16x128b_x16(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), KB_V8(0), KB_V8(8), KB_V8(16), KB_V8(24)
+      : "memory");
+}
+#undef KB_V8
 
 // ---------------------------------------------------------------- arithmetic
 
