@@ -45,8 +45,8 @@ struct PackedCfg {
   static constexpr int kBarVFull = kBarKEmpty + kStages;
   static constexpr int kBarVEmpty = kBarVFull + kStages;
   static constexpr int kBarSFull = kBarVEmpty + kStages;   // one per S buffer
-  static constexpr int kBarPFull = kBarSFull + kSBufs;
-  static constexpr int kBarOFull = kBarPFull + 1;          // one per S buffer: P V of a tile using it done
+  static constexpr int kBarPFull = kBarSFull + kSBufs;     // one per S buffer: P of a tile using it written
+  static constexpr int kBarOFull = kBarPFull + kSBufs;     // one per S buffer: P V of a tile using it done
   static constexpr int kBarVReady = kBarOFull + kSBufs;    // last V tile with its tail zeroed
   static constexpr int kBarDrain = kBarVReady + 1;
   static constexpr int kNumBars = kBarDrain + 1;
@@ -150,7 +150,8 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::kNumBars; ++i)
-      mbar_init(bar(i), i == Cfg::kBarPFull ? static_cast<uint32_t>(32 * Cfg::kSoftmaxWarps) : 1u);
+      mbar_init(bar(i), (i >= Cfg::kBarPFull && i < Cfg::kBarPFull + Cfg::kSBufs)
+                            ? static_cast<uint32_t>(32 * Cfg::kSoftmaxWarps) : 1u);
     misc[1] = (*reinterpret_cast<volatile uint32_t*>(args.err) != 0) ? 1u : 0u;
     fence_mbar_init();
   }
@@ -257,7 +258,8 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           tc_commit(bar(Cfg::kBarKEmpty + slot));
         }
         const int slot = j % Cfg::kStages;
-        ok = mbar_wait(bar(Cfg::kBarPFull), j & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        ok = mbar_wait(bar(Cfg::kBarPFull + j % Cfg::kSBufs), (j / Cfg::kSBufs) & 1, abort_flag, args.err,
+                       kDevTimeoutSoftmax);
         if (ok) {
           if (zero_tail && j == n_kv - 1)
             ok = mbar_wait(bar(Cfg::kBarVReady), 0, abort_flag, args.err, kDevTimeoutTma);
@@ -327,7 +329,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(Cfg::kBarPFull));
+      mbar_arrive(bar(Cfg::kBarPFull + j % Cfg::kSBufs));
     }
     if (ok)
       ok = mbar_wait(bar(Cfg::kBarOFull + (n_kv - 1) % Cfg::kSBufs), ((n_kv - 1) / Cfg::kSBufs) & 1, abort_flag,
@@ -413,7 +415,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(Cfg::kBarPFull));
+      mbar_arrive(bar(Cfg::kBarPFull + j % Cfg::kSBufs));
     }
     if (ok)
       ok = mbar_wait(bar(Cfg::kBarOFull + (n_kv - 1) % Cfg::kSBufs), ((n_kv - 1) / Cfg::kSBufs) & 1, abort_flag,

@@ -139,15 +139,16 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   if (L < 1 || start < 0 || kv_cap < 1) return KB_ERR_INVALID_ARG;
   if (static_cast<long long>(start) + L > kv_cap) return KB_ERR_INVALID_ARG;
   if (kv_cap > kMaxRows) return KB_ERR_UNSUPPORTED;
-  if (q_tiles_per_cta < 0 || q_tiles_per_cta > 2) return KB_ERR_INVALID_ARG;
+  if (q_tiles_per_cta < 0 || q_tiles_per_cta > kb::kShapeOneTileTwoS) return KB_ERR_INVALID_ARG;
   if (q_tiles_per_cta == 0 && L > kb::kMaxPackedRows) return KB_ERR_INVALID_ARG;
   // a ragged batch sizes the grid for its longest possible sequence
   const int first_tile = ragged ? 0 : start / kb::kTileRows;
   const int last_tile = ragged ? (L + kb::kTileRows - 2) / kb::kTileRows : (start + L - 1) / kb::kTileRows;
-  // CTAs: tile kernel one per (query tile, batch, head group); packed kernel
-  // at most two per (batch, KV head)
+  // CTAs: tile kernels one per (query tile, batch, head group of 1 or 2
+  // heads); packed kernel at most two per (batch, KV head)
+  const int heads_per_cta = q_tiles_per_cta == 2 ? 2 : 1;
   const long long grid = q_tiles_per_cta > 0
-                             ? static_cast<long long>(last_tile - first_tile + 1) * B * (Hq / q_tiles_per_cta)
+                             ? static_cast<long long>(last_tile - first_tile + 1) * B * (Hq / heads_per_cta)
                              : 2LL * B * Hkv;
   if (grid > 0x7FFFFFFFLL) return KB_ERR_UNSUPPORTED;
 
@@ -228,7 +229,9 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
     a.num_pages = paging->num_pages;
   }
   a.err = dst->err;
-  const cudaError_t e = kb::launch_prefill(q_tiles_per_cta, tq, tk, tv, a, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = q_tiles_per_cta == kb::kShapeOneTileTwoS
+                            ? kb::launch_prefill_s2(tq, tk, tv, a, static_cast<cudaStream_t>(stream))
+                            : kb::launch_prefill(q_tiles_per_cta, tq, tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return KB_OK;
 }

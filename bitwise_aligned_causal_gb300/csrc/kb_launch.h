@@ -45,6 +45,11 @@ constexpr int kMaxPackedRows = 32;   // query rows per (batch, head) the packed 
 // (two heads of one GQA group share every K/V tile).
 cudaError_t launch_prefill(int q_tiles_per_cta, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillArgs& a, cudaStream_t s);
+// One 128-row query tile per CTA, one CTA per SM, two S buffers in TMEM so
+// Q K^T of the next key tile overlaps the softmax (CTA shape 3).
+constexpr int kShapeOneTileTwoS = 3;
+cudaError_t launch_prefill_s2(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const PrefillArgs& a, cudaStream_t s);
 // n_sub: 1, or 2 when the chunk crosses a 128-position tile boundary.
 cudaError_t launch_packed(const CUtensorMap& tk, const CUtensorMap& tv, const PackedArgs& a, int n_sub,
                           cudaStream_t s);

@@ -1,0 +1,385 @@
+// kb_prefill2.cu -- causal GQA forward for a block of query rows against a KV
+// cache (prefill and partitioned forward, as kb_prefill.cu), one 128-row
+// query tile per CTA with three S buffers in TMEM, so Q K^T of the next KV
+// tiles runs on the tensor core while the softmax of the current one runs on
+// the SM (KernelBraid README, "Method": GPU-specific tiling, data movement and
+// parallelism are optimised within the numerical contract).
+//
+// The softmax of a row is spread over a quad of four threads through the
+// 16x256b TMEM load (thread u holds keys 8r+2u, 8r+2u+1 of every group of 8,
+// exactly the keys of the contract's partial sums k mod 8 = 2u, 2u+1), so the
+// row math is the contract's, bit for bit (row_softmax_tile_quad).
+//   warps 0..7  softmax: warp w owns TMEM lanes 32(w%4) + 16(w/4) .. +15;
+//               thread t of it rows lane t/4 and lane t/4 + 8 of that block
+//   warp 8      TMA producer of Q and the K ring (lane 0 issues)
+//   warp 9      TMEM allocator + Q K^T issuer (one lane)
+//   warp 10     TMA producer of the V ring (the warp zeroes a V tail)
+//   warp 11     P V issuer (one lane)
+// TMEM: S0 [0,128), S1 [128,256), S2 [256,384), O [384,512); P of a tile
+// overwrites the first 64 columns of its S buffer.
+#include "kb_contract.cuh"
+#include "kb_launch.h"
+
+namespace kb {
+
+struct Prefill2Cfg {
+  static constexpr int kThreads = 384;
+  static constexpr int kLoadWarpK = 8;
+  static constexpr int kMmaWarp = 9;                        // TMEM allocator + Q K^T issuer
+  static constexpr int kLoadWarpV = 10;
+  static constexpr int kPvWarp = 11;                        // P V issuer
+  static constexpr int kStages = 3;
+  static constexpr int kSBufs = 3;                          // = kStages: K slot j%3 frees when S(j) lands
+  static constexpr uint32_t kTmemCols = 512;                // S0, S1, S2, O (128 columns each)
+  static constexpr uint32_t kOCol = kSBufs * 128u;
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kKOff = kTileBytes;
+  static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
+  static constexpr uint32_t kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kBarQFull = 0;
+  static constexpr int kBarKFull = 1;
+  static constexpr int kBarVFull = kBarKFull + kStages;
+  // per S buffer j%3: S(j) written (also: K slot j%3 free), P(j) written
+  // (256 arrivals), P V(j) finished (also: V slot j%3 free)
+  static constexpr int kBarSFull = kBarVFull + kStages;
+  static constexpr int kBarPFull = kBarSFull + kSBufs;
+  static constexpr int kBarOFull = kBarPFull + kSBufs;
+  static constexpr int kBarVReady = kBarOFull + kSBufs;    // last V tile with its tail zeroed
+  static constexpr int kBarDrain = kBarVReady + 1;         // 2: one per MMA issuer
+  static constexpr int kNumBars = kBarDrain + 2;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kSmemUsed = kMiscOff + 16;
+  static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;
+};
+
+__device__ __forceinline__ void drain_wait2(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > 50000000ull) break;
+}
+
+__global__ void __launch_bounds__(Prefill2Cfg::kThreads, 1)
+kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs args) {
+  using Cfg = Prefill2Cfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_addr(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOff);
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kMiscOff);
+  volatile uint32_t* abort_flag = misc + 1;
+  auto bar = [&](int i) { return smem_addr(bars + i); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work unit (b, h, absolute query tile t), longest tiles first; neighbouring
+  // CTAs share (b, t) so a GQA group's heads read the same K/V tiles together.
+  const int tile_rank = blockIdx.x / (args.B * args.Hq);
+  const int rem = blockIdx.x % (args.B * args.Hq);
+  const int b = rem / args.Hq;
+  const int h = rem % args.Hq;
+  const int g = h / kGroup;
+  int start = args.start, L = args.L, first_tile = args.first_tile, n_tiles = args.n_tiles;
+  if (args.starts != nullptr) {
+    start = args.starts[b];
+    L = args.lens[b];
+    if (start < 0 || L < 0 || L > args.L || start + L > args.kv_cap) {
+      if (threadIdx.x == 0) atomicCAS(args.err, 0u, static_cast<uint32_t>(kDevBadInput));
+      return;
+    }
+    if (L == 0) return;
+    first_tile = start / kTileRows;
+    n_tiles = (start + L - 1) / kTileRows - first_tile + 1;
+  }
+  if (tile_rank >= n_tiles) return;
+  const int t = first_tile + n_tiles - 1 - tile_rank;
+  const int n_kv = t + 1;                                          // C1: KV tiles 0..t
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Cfg::kNumBars; ++i)
+      mbar_init(bar(i), (i >= Cfg::kBarPFull && i < Cfg::kBarPFull + Cfg::kSBufs) ? 256u : 1u);
+    misc[1] = (*reinterpret_cast<volatile uint32_t*>(args.err) != 0) ? 1u : 0u;
+    fence_mbar_init();
+  }
+  if (warp == Cfg::kMmaWarp) {
+    tmem_alloc(sbase + Cfg::kMiscOff, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const bool skip = (*abort_flag != 0);
+  const bool paged = args.block_table != nullptr;
+  const int kv_len = start + L;
+  const bool zero_tail = paged || (args.starts != nullptr);
+
+  if (warp == Cfg::kLoadWarpK || warp == Cfg::kLoadWarpV) {
+    // ----------------------------------------------------------- producers
+    // One warp per ring (K with Q; V with the tail zeroing), so that each ring
+    // runs kStages tiles ahead of its own consumer: K(j+2) is wanted right
+    // after P V(j), long before V(j+1)'s slot frees.
+    const bool is_v = (warp == Cfg::kLoadWarpV);
+    if (!skip) {
+      const uint64_t keep = l2_policy_evict_last();
+      const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
+      const int full0 = is_v ? Cfg::kBarVFull : Cfg::kBarKFull;
+      const int empty0 = is_v ? Cfg::kBarOFull : Cfg::kBarSFull;   // slot j%3 free: P V(j) / Q K^T(j) done
+      const uint32_t ring = sbase + (is_v ? Cfg::kVOff : Cfg::kKOff);
+      if (lane == 0) {
+        tma_prefetch_desc(tmap);
+        if (!is_v) {
+          tma_prefetch_desc(&tmap_q);
+          mbar_arrive_expect_tx(bar(Cfg::kBarQFull), kTileBytes);
+          tma_load_tile(sbase + Cfg::kQOff, &tmap_q, t * kTileRows - start, b * args.Hq + h, bar(Cfg::kBarQFull));
+        }
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n_kv; ++j) {
+        const int slot = j % Cfg::kStages;
+        const uint32_t use = j / Cfg::kStages;
+        int row = j * kTileKeys, plane = b * args.Hkv + g;
+        if (paged && lane == 0) {
+          int pg = args.block_table[static_cast<size_t>(b) * args.pages_per_seq + row / args.page_size];
+          if (pg < 0 || pg >= args.num_pages) {
+            atomicCAS(args.err, 0u, static_cast<uint32_t>(kDevBadInput));
+            pg = args.num_pages;       // beyond the map: the TMA unit reads zeros
+          }
+          row = row % args.page_size;
+          plane = pg * args.Hkv + g;
+        }
+        if (j >= Cfg::kStages)
+          ok = mbar_wait(bar(empty0 + slot), (use - 1) & 1, abort_flag, args.err, kDevTimeoutSlot);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(full0 + slot), kTileBytes);
+          tma_load_tile_hint(ring + slot * kTileBytes, tmap, row, plane, bar(full0 + slot), keep);
+        }
+        issued = j + 1;
+      }
+      if (ok && is_v && zero_tail) {
+        // V rows past kv_len in the last tile may hold anything: zero them
+        const int jl = n_kv - 1;
+        const int slot = jl % Cfg::kStages;
+        ok = mbar_wait(bar(Cfg::kBarVFull + slot), (jl / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          uint8_t* vt = smem + Cfg::kVOff + slot * kTileBytes;
+          const int tail_from = min(kTileKeys, kv_len - jl * kTileKeys);
+          for (int idx = tail_from * 16 + lane; idx < kTileKeys * 16; idx += 32) {
+            const int vr = idx >> 4;
+            const int c = idx & 15;
+            *reinterpret_cast<uint4*>(vt + (c >> 3) * kSlabBytes + (vr >> 3) * 1024 + (vr & 7) * 128 +
+                                      (((c & 7) ^ (vr & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(Cfg::kBarVReady));
+        }
+      }
+      if (!ok && lane == 0) {
+        if (!is_v) drain_wait2(bar(Cfg::kBarQFull), 0);
+        for (int x = (issued > Cfg::kStages ? issued - Cfg::kStages : 0); x < issued; ++x)
+          drain_wait2(bar(full0 + x % Cfg::kStages), (x / Cfg::kStages) & 1);
+      }
+    }
+  } else if (warp == Cfg::kMmaWarp) {
+    // -------------------------------------------------------- Q K^T issuer
+    // S(j) goes to buffer j%3 once P V(j-3) has read P(j-3) there.  A second
+    // thread issues P V, so that the tensor pipe always has the other
+    // stream's instructions while one issuer waits on a barrier.
+    static_assert(Cfg::kSBufs == Cfg::kStages, "slot and buffer indices coincide");
+    if (lane == 0 && !skip) {
+      const uint32_t q_saddr = sbase + Cfg::kQOff;
+      bool ok = mbar_wait(bar(Cfg::kBarQFull), 0, abort_flag, args.err, kDevTimeoutTma);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int sb = j % Cfg::kSBufs;
+        const uint32_t use = j / Cfg::kSBufs;
+        ok = mbar_wait(bar(Cfg::kBarKFull + sb), use & 1, abort_flag, args.err, kDevTimeoutTma);
+        if (ok && j >= Cfg::kSBufs)
+          ok = mbar_wait(bar(Cfg::kBarOFull + sb), (use - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
+        if (!ok) break;
+        tc_fence_after();
+        issue_qk(tmem_base + sb * 128u, q_saddr, 1024u, kSlabBytes, sbase + Cfg::kKOff + sb * kTileBytes);
+        tc_commit(bar(Cfg::kBarSFull + sb));
+      }
+      if (!ok) {
+        tc_commit(bar(Cfg::kBarDrain));
+        drain_wait2(bar(Cfg::kBarDrain), 0);
+      }
+    }
+  } else if (warp == Cfg::kPvWarp) {
+    // ---------------------------------------------------------- P V issuer
+    if (lane == 0 && !skip) {
+      bool ok = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int sb = j % Cfg::kSBufs;
+        const uint32_t use = j / Cfg::kSBufs;
+        ok = mbar_wait(bar(Cfg::kBarPFull + sb), use & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        if (ok) {
+          if (zero_tail && j == n_kv - 1)
+            ok = mbar_wait(bar(Cfg::kBarVReady), 0, abort_flag, args.err, kDevTimeoutTma);
+          else
+            ok = mbar_wait(bar(Cfg::kBarVFull + sb), use & 1, abort_flag, args.err, kDevTimeoutTma);
+        }
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(tmem_base + Cfg::kOCol, tmem_base + sb * 128u, sbase + Cfg::kVOff + sb * kTileBytes, j == 0);
+        tc_commit(bar(Cfg::kBarOFull + sb));
+      }
+      if (!ok) {
+        tc_commit(bar(Cfg::kBarDrain + 1));
+        drain_wait2(bar(Cfg::kBarDrain + 1), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int q4 = warp & 3;                                        // TMEM lane quarter of this warp
+    const int lane_base = 32 * q4 + 16 * (warp >> 2);               // 16-lane block
+    const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
+    const int u = lane & 3;
+    const int rA = lane_base + (lane >> 2);                         // rows (TMEM lanes) of this thread
+    const int rB = rA + 8;
+    const uint32_t o_tmem = tmem_base + Cfg::kOCol + lane_off;
+    RowState sA = row_state_init();
+    RowState sB = row_state_init();
+    bool ok = !skip;
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int sb = j % Cfg::kSBufs;
+      ok = mbar_wait(bar(Cfg::kBarSFull + sb), (j / Cfg::kSBufs) & 1, abort_flag, args.err, kDevTimeoutMma);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t s_tmem = tmem_base + sb * 128u + lane_off;
+      float xA[32], xB[32];
+      {
+        uint32_t v[32];
+        tmem_ld_16x256b_x8_wait(s_tmem, v);                         // keys 0..63
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          xA[2 * r] = __uint_as_float(v[4 * r]);
+          xA[2 * r + 1] = __uint_as_float(v[4 * r + 1]);
+          xB[2 * r] = __uint_as_float(v[4 * r + 2]);
+          xB[2 * r + 1] = __uint_as_float(v[4 * r + 3]);
+        }
+        tmem_ld_16x256b_x8_wait(s_tmem + 64u, v);                   // keys 64..127
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          xA[16 + 2 * r] = __uint_as_float(v[4 * r]);
+          xA[16 + 2 * r + 1] = __uint_as_float(v[4 * r + 1]);
+          xB[16 + 2 * r] = __uint_as_float(v[4 * r + 2]);
+          xB[16 + 2 * r + 1] = __uint_as_float(v[4 * r + 3]);
+        }
+      }
+      uint32_t pA[16], pB[16];
+      float aA, aB;
+      if (j == n_kv - 1) {                                          // diagonal tile: causal mask
+        aA = row_softmax_tile_quad<true>(xA, u, rA + 1, sA, pA);
+        aB = row_softmax_tile_quad<true>(xB, u, rB + 1, sB, pB);
+      } else {
+        aA = row_softmax_tile_quad<false>(xA, u, kTileKeys, sA, pA);
+        aB = row_softmax_tile_quad<false>(xB, u, kTileKeys, sB, pB);
+      }
+      if (j > 0 && __any_sync(0xffffffffu, aA != 1.0f || aB != 1.0f)) {
+        // O must hold P V of tile j-1 before it is rescaled; per-buffer
+        // barriers keep this wait exact although it is only taken when needed
+        // (P V(j-4) is done: S(j) was committed after it)
+        ok = mbar_wait(bar(Cfg::kBarOFull + (j - 1) % Cfg::kSBufs), ((j - 1) / Cfg::kSBufs) & 1, abort_flag,
+                       args.err, kDevTimeoutMma);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t o[32];
+          tmem_ld_16x256b_x8_wait(o_tmem + 64u * half, o);
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const float2 ra = __fmul2_rn(make_float2(__uint_as_float(o[4 * r]), __uint_as_float(o[4 * r + 1])),
+                                         make_float2(aA, aA));
+            const float2 rb = __fmul2_rn(make_float2(__uint_as_float(o[4 * r + 2]), __uint_as_float(o[4 * r + 3])),
+                                         make_float2(aB, aB));
+            o[4 * r] = __float_as_uint(ra.x);
+            o[4 * r + 1] = __float_as_uint(ra.y);
+            o[4 * r + 2] = __float_as_uint(rb.x);
+            o[4 * r + 3] = __float_as_uint(rb.y);
+          }
+          tmem_st_16x256b_x8(o_tmem + 64u * half, o);
+        }
+      }
+      {
+        uint32_t pv[32];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) { pv[2 * r] = pA[r]; pv[2 * r + 1] = pB[r]; }
+        tmem_st_16x128b_x16(s_tmem, pv);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(Cfg::kBarPFull + sb));
+    }
+    if (ok)
+      ok = mbar_wait(bar(Cfg::kBarOFull + (n_kv - 1) % Cfg::kSBufs), ((n_kv - 1) / Cfg::kSBufs) & 1, abort_flag,
+                     args.err, kDevTimeoutMma);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      const float invA = row_inv_l(sA);
+      const float invB = row_inv_l(sB);
+      const int iA = t * kTileRows + rA - start;                     // query row index in q / o
+      const int iB = iA + 8;
+      const bool stA = (iA >= 0) && (iA < L);
+      const bool stB = (iB >= 0) && (iB < L);
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.o) + (static_cast<size_t>(b) * args.Hq + h) *
+                                                                       static_cast<size_t>(args.L) * kHeadDim;
+      uint32_t* dA = reinterpret_cast<uint32_t*>(orow + static_cast<size_t>(stA ? iA : 0) * kHeadDim);
+      uint32_t* dB = reinterpret_cast<uint32_t*>(orow + static_cast<size_t>(stB ? iB : 0) * kHeadDim);
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t o[32];
+        tmem_ld_16x256b_x8_wait(o_tmem + 64u * half, o);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int col = 64 * half + 8 * r + 2 * u;                 // this thread's two columns
+          const uint32_t wa = pack_bf16x2(__fmul_rn(__uint_as_float(o[4 * r]), invA),
+                                          __fmul_rn(__uint_as_float(o[4 * r + 1]), invA));
+          const uint32_t wb = pack_bf16x2(__fmul_rn(__uint_as_float(o[4 * r + 2]), invB),
+                                          __fmul_rn(__uint_as_float(o[4 * r + 3]), invB));
+          if (stA) dA[col >> 1] = wa;
+          if (stB) dB[col >> 1] = wb;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == Cfg::kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+cudaError_t launch_prefill_s2(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const PrefillArgs& a, cudaStream_t s) {
+  using Cfg = Prefill2Cfg;
+  static_assert(Cfg::kSmemBytes <= 227u * 1024u, "shared memory budget");
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(kb_prefill_kernel_s2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Cfg::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const long long grid = static_cast<long long>(a.n_tiles) * a.B * a.Hq;
+  kb_prefill_kernel_s2<<<static_cast<unsigned>(grid), Cfg::kThreads, Cfg::kSmemBytes, s>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace kb

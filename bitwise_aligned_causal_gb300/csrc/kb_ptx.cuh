@@ -333,6 +333,19 @@ __device__ __forceinline__ void tmem_ld_16x256b_x8_wait(uint32_t taddr, uint32_t
 }
 #undef KB_R8
 
+// 16x256b shape, 8 repetitions (the store of the load above).
+#define KB_V8(b) "r"(v[b + 0]), "r"(v[b + 1]), "r"(v[b + 2]), "r"(v[b + 3]), \
+                 "r"(v[b + 4]), "r"(v[b + 5]), "r"(v[b + 6]), "r"(v[b + 7])
+__device__ __forceinline__ void tmem_st_16x256b_x8(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), KB_V8(0), KB_V8(8), KB_V8(16), KB_V8(24)
+      : "memory");
+}
+#undef KB_V8
+
 // 16x128b shape, 16 repetitions: thread t writes lanes base + t/4 (register
 // 2r) and base + t/4 + 8 (register 2r+1), column 4r + t%4 of repetition r.
 #define KB_V8(b) "r"(v[b + 0]), "r"(v[b + 1]), "r"(v[b + 2]), "r"(v[b + 3]), \

@@ -113,14 +113,17 @@ def test_cache_rows_beyond_context_are_ignored(kb):
     assert np.array_equal(c[:, :, 0], a[:, :, S - 1])
 
 
-def test_cta_shapes_give_identical_bits(kb):
-    """One or two query tiles per CTA: same contract, same bits."""
-    x = inputs.make_qkv(2, 700, seed=40_000)
+@pytest.mark.parametrize("S", [700, 1300])
+def test_cta_shapes_give_identical_bits(kb, S):
+    """One or two query tiles per CTA, one or two score buffers: same contract, same bits."""
+    x = inputs.make_qkv(2, S, seed=40_000 + S)
     q, k, v = to_dev(x.q), to_dev(x.k), to_dev(x.v)
     a = from_dev(kb.chunk(q, k, v, 0, q_tiles_per_cta=1))
     b = from_dev(kb.chunk(q, k, v, 0, q_tiles_per_cta=2))
+    c = from_dev(kb.chunk(q, k, v, 0, q_tiles_per_cta=3))
     kb.check_device_status()
     assert np.array_equal(a, b)
+    assert np.array_equal(a, c)
 
 
 def test_repeat_runs_are_identical(kb):
