@@ -346,6 +346,27 @@ def pipelined_e2e(n, host_in, dev_sets, host_out, launch):
     return t0.elapsed_time(t1) / n
 
 
+def link_bandwidth(host_in, dev_in, host_out, dev_out):
+    """Host<->device copy bandwidth alone (GB/s): the prefill inputs uploaded,
+    its output downloaded, each timed on its own."""
+    import torch
+
+    st = torch.cuda.Stream()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        e0.record(st)
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        e1.record(st)
+        host_out.copy_(dev_out, non_blocking=True)
+        e2.record(st)
+    torch.cuda.synchronize()
+    up = sum(h.numel() * h.element_size() for h in host_in)
+    down = host_out.numel() * host_out.element_size()
+    return up / (e0.elapsed_time(e1) * 1e6), down / (e1.elapsed_time(e2) * 1e6)
+
+
 def run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_attn):
     import numpy as np
     import torch
@@ -370,6 +391,7 @@ def run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_att
     dec_ms = pipelined_e2e(n, [hqd, hkd, hvd], dec_sets, hod,
                            lambda ins, out: kb_attn.decode(ins[0], ins[1], ins[2], DECODE_CTX, out=out))
     kb_attn.check_device_status()
+    h2d_gbs, d2h_gbs = link_bandwidth([hq, hk, hv], pre_sets[1][0], ho[0], o)
     # the downloaded results are the kernels' results
     assert torch.equal(ho[(n - 1) % 2].view(torch.int16), o.view(torch.int16).cpu())
     e2e_pre_ms = reduce_max(pre_ms, world, "cuda" if world > 1 else "cpu")
@@ -379,8 +401,10 @@ def run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_att
     return {"value": aggregate(pf, world, e2e_pre_ms / 1e3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "decode_gbs": aggregate(db, world, e2e_dec_ms / 1e3) / 1e9, "steps": n,
+            "copy_only_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs},
             "note": ("every step uploads its inputs from pinned host memory and downloads its output; "
-                     "two buffer sets let one step's copies overlap the neighbouring step's kernels")}
+                     "two buffer sets let one step's copies overlap the neighbouring step's kernels; "
+                     "bound by the host link when (h2d + d2h bytes) / copy_only_gbs exceeds the kernel time")}
 
 
 def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks,
@@ -428,7 +452,7 @@ def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_ma
         "roofline": {
             "bound": "tensor", "achieved": pre_per_launch, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": pre_per_launch / peaks["bf16_tflops"], "traffic": tr_pre,
-            "kernel": "kb_prefill_kernel", "peak_source": peaks["source"] + " burst bf16",
+            "kernel": "kb_prefill_kernel_s2", "peak_source": peaks["source"] + " burst bf16",
             "frac_of_sustained": pre_per_launch / peaks["bf16_tflops_sustained"],
         },
         "cpu_baseline": cpu,

@@ -23,6 +23,7 @@ __device__ uint32_t g_kb_error_word;
 
 struct DeviceState {
   uint32_t* err = nullptr;
+  int sm_count = 0;
   bool ready = false;
 };
 DeviceState g_dev[kMaxDevices];
@@ -48,6 +49,8 @@ kb_status get_device_state(DeviceState** out) {
     void* p = nullptr;
     if ((e = cudaGetSymbolAddress(&p, g_kb_error_word)) != cudaSuccess) return cuda_fail(e);
     st.err = static_cast<uint32_t*>(p);
+    if ((e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
     st.ready = true;
   }
   if (!g_encode) {
@@ -139,7 +142,7 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   if (L < 1 || start < 0 || kv_cap < 1) return KB_ERR_INVALID_ARG;
   if (static_cast<long long>(start) + L > kv_cap) return KB_ERR_INVALID_ARG;
   if (kv_cap > kMaxRows) return KB_ERR_UNSUPPORTED;
-  if (q_tiles_per_cta < 0 || q_tiles_per_cta > kb::kShapeOneTileTwoS) return KB_ERR_INVALID_ARG;
+  if (q_tiles_per_cta < 0 || q_tiles_per_cta > kb::kShapeOneTilePerSm) return KB_ERR_INVALID_ARG;
   if (q_tiles_per_cta == 0 && L > kb::kMaxPackedRows) return KB_ERR_INVALID_ARG;
   // a ragged batch sizes the grid for its longest possible sequence
   const int first_tile = ragged ? 0 : start / kb::kTileRows;
@@ -218,6 +221,9 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   a.first_tile = first_tile;
   a.n_tiles = last_tile - first_tile + 1;
   a.kv_cap = kv_cap;
+  // beyond a few waves, order CTAs by GQA group so that the resident ones
+  // share K/V in L2; below that, globally longest tile first
+  a.group_major = grid > 4LL * dst->sm_count ? 1 : 0;
   if (ragged) {
     a.starts = ragged->starts;
     a.lens = ragged->lens;
@@ -229,14 +235,14 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
     a.num_pages = paging->num_pages;
   }
   a.err = dst->err;
-  const cudaError_t e = q_tiles_per_cta == kb::kShapeOneTileTwoS
+  const cudaError_t e = q_tiles_per_cta == kb::kShapeOneTilePerSm
                             ? kb::launch_prefill_s2(tq, tk, tv, a, static_cast<cudaStream_t>(stream))
                             : kb::launch_prefill(q_tiles_per_cta, tq, tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return KB_OK;
 }
 
-constexpr int kDefaultQTilesPerCta = 1;
+constexpr int kDefaultQTilesPerCta = kb::kShapeOneTilePerSm;
 
 // Chunks of at most this many query rows go to the packed kernel.
 int chunk_cta_shape(int L) { return L <= kb::kMaxPackedRows ? 0 : kDefaultQTilesPerCta; }

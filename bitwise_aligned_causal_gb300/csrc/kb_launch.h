@@ -20,6 +20,7 @@ struct PrefillArgs {
   const int* starts;       // optional device [B]: per-sequence start (ragged batch; then
   const int* lens;         //   L is the row stride of q and o and lens[b] <= L rows are used)
   int kv_cap;              // keys per sequence the cache can hold
+  int group_major;         // CTA order: 1 = (b, g) slowest, 0 = query tile slowest
   uint32_t* err;    // device error word
 };
 
@@ -45,9 +46,10 @@ constexpr int kMaxPackedRows = 32;   // query rows per (batch, head) the packed 
 // (two heads of one GQA group share every K/V tile).
 cudaError_t launch_prefill(int q_tiles_per_cta, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillArgs& a, cudaStream_t s);
-// One 128-row query tile per CTA, one CTA per SM, two S buffers in TMEM so
-// Q K^T of the next key tile overlaps the softmax (CTA shape 3).
-constexpr int kShapeOneTileTwoS = 3;
+// One 128-row query tile per CTA, one CTA per SM, three S buffers in TMEM
+// and separate Q K^T / P V issuers, so the tensor pipe works on later key
+// tiles while the softmax runs (CTA shape 3).
+constexpr int kShapeOneTilePerSm = 3;
 cudaError_t launch_prefill_s2(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const PrefillArgs& a, cudaStream_t s);
 // n_sub: 1, or 2 when the chunk crosses a 128-position tile boundary.

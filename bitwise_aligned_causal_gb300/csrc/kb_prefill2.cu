@@ -73,13 +73,26 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work unit (b, h, absolute query tile t), longest tiles first; neighbouring
-  // CTAs share (b, t) so a GQA group's heads read the same K/V tiles together.
-  const int tile_rank = blockIdx.x / (args.B * args.Hq);
-  const int rem = blockIdx.x % (args.B * args.Hq);
-  const int b = rem / args.Hq;
-  const int h = rem % args.Hq;
-  const int g = h / kGroup;
+  // Work unit (b, h, absolute query tile t), a GQA group's four heads
+  // adjacent.  Group-major order: (b, g) slowest, so the CTAs resident at one
+  // time share one group's K/V in L2, query tiles longest first within it.
+  // Otherwise the query tile is slowest (longest first over the whole grid).
+  int b, g, h, tile_rank;
+  if (args.group_major) {
+    const int units_per_group = args.n_tiles * kGroup;
+    const int bg = blockIdx.x / units_per_group;
+    const int rem = blockIdx.x % units_per_group;
+    tile_rank = rem / kGroup;
+    b = bg / args.Hkv;
+    g = bg % args.Hkv;
+    h = g * kGroup + rem % kGroup;
+  } else {
+    tile_rank = blockIdx.x / (args.B * args.Hq);
+    const int rem = blockIdx.x % (args.B * args.Hq);
+    b = rem / args.Hq;
+    h = rem % args.Hq;
+    g = h / kGroup;
+  }
   int start = args.start, L = args.L, first_tile = args.first_tile, n_tiles = args.n_tiles;
   if (args.starts != nullptr) {
     start = args.starts[b];

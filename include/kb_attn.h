@@ -161,10 +161,10 @@ kb_status kb_attn_debug_wait_timeout(int limit_us, void* stream);
  * Prefill/chunk with an explicit kernel shape, for tests of the contract:
  * q_tiles_per_cta = 1 or 2 runs the tile kernel with that many 128-row query
  * tiles per CTA; 3 runs the tile kernel with one query tile per CTA, one CTA
- * per SM and two score buffers (Q K^T of the next key tile overlaps the
+ * per SM and three score buffers (Q K^T of later key tiles overlaps the
  * softmax of the current one); 0 runs the packed kernel (the 4 heads of a GQA group times
  * the chunk's rows in one MMA tile; L <= 32).  kb_attn_chunk, kb_attn_prefill
- * and kb_attn_decode pick packed for L <= 32 and 1 otherwise.  Every shape
+ * and kb_attn_decode pick packed for L <= 32 and 3 otherwise.  Every shape
  * gives the same bits.
  */
 kb_status kb_attn_chunk_cta_shape(const void* q, const void* k, const void* v, void* o,
