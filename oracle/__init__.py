@@ -5,11 +5,15 @@ benchmark's CPU-baseline leg are the only callers.  The CUDA library never
 imports, links or runs anything here, and this package never touches it.
 
 The arithmetic lives in ``kb_oracle.c`` (plain definition of causal GQA
-attention in double precision; see the header of that file).  This module
+attention in double precision, and of its gradient with respect to q, k
+and v; see the comments in that file).  This module
 only builds it with gcc, loads it with ctypes and marshals numpy arrays.
 
-Parity status: pinned.  ``tests/test_oracle_pins.py`` checks it against
-closed forms, invariants of the definition and an independent brute force.
+Parity status: pinned.  ``tests/test_oracle_pins.py`` checks the forward
+against closed forms, invariants of the definition and an independent brute
+force; ``tests/test_oracle_backward_pins.py`` checks the gradient against
+central finite differences of the forward oracle, float64 autograd of an
+independent PyTorch expression, closed forms and invariants.
 """
 
 from __future__ import annotations
@@ -46,6 +50,18 @@ def _bind(path: str):
         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_int,
         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+    ]
+    lib.kb_oracle_backward.restype = ctypes.c_int
+    lib.kb_oracle_backward.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+    ]
+    lib.kb_oracle_dq_rows.restype = ctypes.c_int
+    lib.kb_oracle_dq_rows.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
     ]
     return lib
 
@@ -106,3 +122,61 @@ def attention_full(q_bits, k_bits, v_bits, *, start: int = 0, n_threads: int | N
     out = attention_rows(q_bits, k_bits, v_bits, rows, start=start, n_threads=n_threads,
                          _lib_override=_lib_override)
     return out.reshape(B, Hq, Lq, D)
+
+
+def _bwd_inputs(q_bits, k_bits, v_bits, dout_bits):
+    q = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    k = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    v = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    do = np.ascontiguousarray(dout_bits, dtype=np.uint16)
+    if q.ndim != 4 or k.ndim != 4 or v.shape != k.shape or do.shape != q.shape:
+        raise ValueError("q, dout must be [B,Hq,S,D] and k, v [B,Hkv,S,D]")
+    B, Hq, S, D = q.shape
+    if k.shape[0] != B or k.shape[2] != S or k.shape[3] != D:
+        raise ValueError("k, v must cover the same batch, sequence and head_dim as q")
+    return q, k, v, do
+
+
+def backward(q_bits, k_bits, v_bits, dout_bits, *, n_threads: int | None = None, _lib_override=None):
+    """Gradients (dq, dk, dv), float64, of causal GQA attention over a whole
+    sequence (query row i at position i) for output gradient ``dout``.
+
+    q_bits, dout_bits: uint16 bf16 bits [B, Hq, S, D]; k_bits, v_bits [B, Hkv, S, D].
+    """
+    lib = _load() if _lib_override is None else _lib_override
+    q, k, v, do = _bwd_inputs(q_bits, k_bits, v_bits, dout_bits)
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    dq = np.empty(q.shape, dtype=np.float64)
+    dk = np.empty(k.shape, dtype=np.float64)
+    dv = np.empty(k.shape, dtype=np.float64)
+    nt = default_threads() if n_threads is None else int(n_threads)
+    rc = lib.kb_oracle_backward(q.ctypes.data, k.ctypes.data, v.ctypes.data, do.ctypes.data,
+                                B, Hq, Hkv, S, D, dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, nt)
+    if rc != 0:
+        raise ValueError(f"kb_oracle_backward failed with code {rc}")
+    return dq, dk, dv
+
+
+def dq_rows(q_bits, k_bits, v_bits, dout_bits, rows, *, n_threads: int | None = None, _lib_override=None):
+    """For listed rows (b, h, i) of a whole-sequence prefill: dq [n, D], the
+    natural-log log-sum-exp of the row's scaled scores [n] and
+    delta = sum_j P_ij dP_ij [n] (float64)."""
+    lib = _load() if _lib_override is None else _lib_override
+    q, k, v, do = _bwd_inputs(q_bits, k_bits, v_bits, dout_bits)
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    n = r.shape[0]
+    dq = np.empty((n, D), dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    delta = np.empty(n, dtype=np.float64)
+    if n == 0:
+        return dq, lse, delta
+    nt = default_threads() if n_threads is None else int(n_threads)
+    rc = lib.kb_oracle_dq_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, do.ctypes.data,
+                               B, Hq, Hkv, S, D, r.ctypes.data, n, dq.ctypes.data, lse.ctypes.data,
+                               delta.ctypes.data, nt)
+    if rc != 0:
+        raise ValueError(f"kb_oracle_dq_rows failed with code {rc}")
+    return dq, lse, delta

@@ -15,6 +15,7 @@ import types
 import pytest
 
 import oracle
+from tests import test_oracle_backward_pins as bwd_pins
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "kb_oracle.c")
@@ -47,6 +48,8 @@ def _mutant_module(tmp_path, old, new):
     mod = types.SimpleNamespace(
         attention_rows=functools.partial(oracle.attention_rows, _lib_override=lib),
         attention_full=functools.partial(oracle.attention_full, _lib_override=lib),
+        backward=functools.partial(oracle.backward, _lib_override=lib),
+        dq_rows=functools.partial(oracle.dq_rows, _lib_override=lib),
     )
     return mod
 
@@ -62,3 +65,37 @@ def test_some_pin_fails_on_mutant(tmp_path, name):
         except Exception as e:  # noqa: BLE001 - any failure of a pin counts
             failures.append(getattr(t, "__name__", "brute_force"))
     assert failures, f"mutant {name} passed every pin"
+
+
+# Slips in the gradient code; the forward code of the mutant is untouched, so
+# the finite-difference pin compares against a correct forward.
+BWD_MUTANTS = {
+    "dropped_delta": ("const double ds = p[j] * (dp[j] - delta);", "const double ds = p[j] * dp[j];"),
+    "dq_missing_scale": ("dqrow[d] += ds * bf16_to_double(krow[d]) * inv_sqrt_d;",
+                         "dqrow[d] += ds * bf16_to_double(krow[d]);"),
+    "dk_uses_dout": ("dkrow[d] += ds * qd[d] * inv_sqrt_d;", "dkrow[d] += ds * dod[d] * inv_sqrt_d;"),
+    "dv_uses_ds": ("dvrow[d] += p[j] * dod[d];", "dvrow[d] += ds * dod[d];"),
+    "delta_unweighted": ("delta += p[j] * dot;", "delta += dot;"),
+    "group_interleaved": ("for (int h = g * group; h < (g + 1) * group; ++h) {",
+                          "for (int h = g; h < J->Hq; h += J->Hkv) {"),
+    "causal_off_by_one": ("softmax_row(qd, kbase, i, D, inv_sqrt_d, p);",
+                          "softmax_row(qd, kbase, i > 0 ? i - 1 : 0, D, inv_sqrt_d, p);"),
+}
+
+BWD_PIN_TESTS = [getattr(bwd_pins, n) for n in dir(bwd_pins) if n.startswith("test_")]
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTANTS))
+def test_some_backward_pin_fails_on_mutant(tmp_path, name):
+    old, new = BWD_MUTANTS[name]
+    mod = _mutant_module(tmp_path, old, new)
+    failures = []
+    for t in BWD_PIN_TESTS:
+        try:
+            if t is bwd_pins.test_finite_differences:
+                t(mod, bwd_pins.make_small_case())
+            else:
+                t(mod)
+        except Exception as e:  # noqa: BLE001 - any failure of a pin counts
+            failures.append(t.__name__)
+    assert failures, f"mutant {name} passed every backward pin"
