@@ -1,0 +1,604 @@
+// kb_backward.cu -- gradient of the causal GQA attention of a whole sequence
+// (KernelBraid README, "Motivation": the policy-update step of RL training
+// differentiates the same attention the rollouts ran forward).
+//
+// With P the row softmax of s = q.k / sqrt(128) over keys 0..i, recomputed
+// from the forward's log-sum-exp, and dO the gradient of the output:
+//   delta_i = dO_i . O_i                     (= sum_j P_ij dP_ij)
+//   dP_ij   = dO_i . v_j
+//   dS_ij   = P_ij (dP_ij - delta_i)
+//   dq_i    = sum_j dS_ij k_j / sqrt(128)
+//   dk_j    = sum over the group's heads and rows i >= j of dS_ij q_i / sqrt(128)
+//   dv_j    = sum over the group's heads and rows i >= j of P_ij dO_i
+//
+// Three kernels, no atomics (every gradient element is summed by one CTA in
+// one fixed order, so repeated runs give the same bits):
+//   kb_bwd_delta_kernel  one warp per row: delta = rowsum(dO * O)
+//   kb_bwd_dq_kernel     one CTA per (b, head, query tile): walks key tiles
+//                        0..t; S = Q K^T and dP = dO V^T on the tensor core,
+//                        dS in TMEM, dQ += dS K
+//   kb_bwd_dkdv_kernel   one CTA per (b, kv head, key tile): walks the four
+//                        heads of the group and query tiles t..n-1;
+//                        S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q
+// Every product uses the two forms of the forward: both operands K-major in
+// shared memory (issue_qk), or A from TMEM and B MN-major (issue_pv).
+#include "kb_contract.cuh"
+#include "kb_launch.h"
+
+namespace kb {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;          // log2(e), to turn a natural-log lse into base 2
+constexpr float kInvSqrtD = 0.088388347648318440f;     // 1 / sqrt(128)
+
+__device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > 50000000ull) break;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+}  // namespace
+
+// ------------------------------------------------------------------ delta
+
+// One warp per row of 128: lane l takes elements 4l..4l+3; the four products
+// are summed in pairs, then across lanes by a fixed butterfly.
+__global__ void __launch_bounds__(256) kb_bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                           const __nv_bfloat16* __restrict__ dout,
+                                                           float* __restrict__ delta, long long rows) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const uint2 a = reinterpret_cast<const uint2*>(o + row * kHeadDim)[lane];
+  const uint2 g = reinterpret_cast<const uint2*>(dout + row * kHeadDim)[lane];
+  const float p01 = __fmaf_rn(bf16_lo(a.x), bf16_lo(g.x), __fmul_rn(bf16_hi(a.x), bf16_hi(g.x)));
+  const float p23 = __fmaf_rn(bf16_lo(a.y), bf16_lo(g.y), __fmul_rn(bf16_hi(a.y), bf16_hi(g.y)));
+  float s = __fadd_rn(p01, p23);
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, m));
+  if (lane == 0) delta[row] = s;
+}
+
+// -------------------------------------------------------------- dq kernel
+
+struct BwdQCfg {
+  static constexpr int kThreads = 320;        // 8 elementwise warps, producer, MMA issuer
+  static constexpr int kLoadWarp = 8;
+  static constexpr int kMmaWarp = 9;
+  static constexpr int kStages = 2;           // K/V ring
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kDOOff = kTileBytes;
+  static constexpr uint32_t kKOff = 2 * kTileBytes;
+  static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
+  static constexpr uint32_t kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kBarQD = 0;                         // Q and dO landed
+  static constexpr int kBarKVFull = 1;                     // 2: K(j), V(j) landed in slot j%2
+  static constexpr int kBarKVEmpty = kBarKVFull + kStages; // 2: dQ(j) done, slot j%2 free
+  static constexpr int kBarSFull = kBarKVEmpty + kStages;  // S(j), dP(j) in TMEM
+  static constexpr int kBarSFree = kBarSFull + 1;          // S(j), dP(j) read (256 arrivals)
+  static constexpr int kBarDSFull = kBarSFree + 1;         // dS(j) in TMEM (256 arrivals)
+  static constexpr int kBarDQDone = kBarDSFull + 1;        // dQ += dS(j) K(j) finished
+  static constexpr int kBarDrain = kBarDQDone + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
+};
+
+__global__ void __launch_bounds__(BwdQCfg::kThreads, 1)
+kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                 const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
+                 const BwdArgs args) {
+  using Cfg = BwdQCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_addr(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOff);
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kMiscOff);
+  volatile uint32_t* abort_flag = misc + 1;
+  auto bar = [&](int i) { return smem_addr(bars + i); };
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // (b, h, query tile t), longest first; group-major beyond a few waves
+  int b, g, h, tile_rank;
+  if (args.group_major) {
+    const int per_group = args.n_tiles * kGroup;
+    const int bg = blockIdx.x / per_group;
+    const int rem = blockIdx.x % per_group;
+    tile_rank = rem / kGroup;
+    b = bg / args.Hkv;
+    g = bg % args.Hkv;
+    h = g * kGroup + rem % kGroup;
+  } else {
+    tile_rank = blockIdx.x / (args.B * args.Hq);
+    const int rem = blockIdx.x % (args.B * args.Hq);
+    b = rem / args.Hq;
+    h = rem % args.Hq;
+    g = h / kGroup;
+  }
+  const int t = args.n_tiles - 1 - tile_rank;
+  const int n_kv = t + 1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Cfg::kNumBars; ++i)
+      mbar_init(bar(i), (i == Cfg::kBarSFree || i == Cfg::kBarDSFull) ? 256u : 1u);
+    misc[1] = (*reinterpret_cast<volatile uint32_t*>(args.err) != 0) ? 1u : 0u;
+    fence_mbar_init();
+  }
+  if (warp == Cfg::kMmaWarp) {
+    tmem_alloc(sbase + Cfg::kMiscOff, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const bool skip = (*abort_flag != 0);
+
+  if (warp == Cfg::kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (!skip) {
+      const uint64_t keep = l2_policy_evict_last();
+      if (lane == 0) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_do);
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+        mbar_arrive_expect_tx(bar(Cfg::kBarQD), 2 * kTileBytes);
+        tma_load_tile(sbase + Cfg::kQOff, &tmap_q, t * kTileRows, b * args.Hq + h, bar(Cfg::kBarQD));
+        tma_load_tile(sbase + Cfg::kDOOff, &tmap_do, t * kTileRows, b * args.Hq + h, bar(Cfg::kBarQD));
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n_kv; ++j) {
+        const int slot = j % Cfg::kStages;
+        if (j >= Cfg::kStages)
+          ok = mbar_wait(bar(Cfg::kBarKVEmpty + slot), ((j / Cfg::kStages) - 1) & 1, abort_flag, args.err,
+                         kDevTimeoutSlot);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(Cfg::kBarKVFull + slot), 2 * kTileBytes);
+          tma_load_tile_hint(sbase + Cfg::kKOff + slot * kTileBytes, &tmap_k, j * kTileRows, b * args.Hkv + g,
+                             bar(Cfg::kBarKVFull + slot), keep);
+          tma_load_tile_hint(sbase + Cfg::kVOff + slot * kTileBytes, &tmap_v, j * kTileRows, b * args.Hkv + g,
+                             bar(Cfg::kBarKVFull + slot), keep);
+        }
+        issued = j + 1;
+      }
+      if (!ok && lane == 0) {
+        drain_wait_b(bar(Cfg::kBarQD), 0);
+        for (int x = (issued > Cfg::kStages ? issued - Cfg::kStages : 0); x < issued; ++x)
+          drain_wait_b(bar(Cfg::kBarKVFull + x % Cfg::kStages), (x / Cfg::kStages) & 1);
+      }
+    }
+  } else if (warp == Cfg::kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    // S(0) dP(0) | S(1) dP(1) [after S(0), dP(0) were read] dQ(0) [after
+    // dS(0)] | S(2) dP(2) dQ(1) | ...  dQ(j) reads K(j) and dS(j) only.
+    if (lane == 0 && !skip) {
+      const uint32_t q_s = sbase + Cfg::kQOff, do_s = sbase + Cfg::kDOOff;
+      bool ok = mbar_wait(bar(Cfg::kBarQD), 0, abort_flag, args.err, kDevTimeoutTma);
+      if (ok) ok = mbar_wait(bar(Cfg::kBarKVFull), 0, abort_flag, args.err, kDevTimeoutTma);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(tmem_base + Cfg::kColS, q_s, 1024u, kSlabBytes, sbase + Cfg::kKOff);
+        issue_qk(tmem_base + Cfg::kColDP, do_s, 1024u, kSlabBytes, sbase + Cfg::kVOff);
+        tc_commit(bar(Cfg::kBarSFull));
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        if (j + 1 < n_kv) {
+          const int s1 = (j + 1) % Cfg::kStages;
+          ok = mbar_wait(bar(Cfg::kBarKVFull + s1), ((j + 1) / Cfg::kStages) & 1, abort_flag, args.err,
+                         kDevTimeoutTma);
+          if (ok) ok = mbar_wait(bar(Cfg::kBarSFree), j & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk(tmem_base + Cfg::kColS, q_s, 1024u, kSlabBytes, sbase + Cfg::kKOff + s1 * kTileBytes);
+          issue_qk(tmem_base + Cfg::kColDP, do_s, 1024u, kSlabBytes, sbase + Cfg::kVOff + s1 * kTileBytes);
+          tc_commit(bar(Cfg::kBarSFull));
+        }
+        ok = mbar_wait(bar(Cfg::kBarDSFull), j & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        if (!ok) break;
+        tc_fence_after();
+        const int s0 = j % Cfg::kStages;
+        issue_pv(tmem_base + Cfg::kColDQ, tmem_base + Cfg::kColDS, sbase + Cfg::kKOff + s0 * kTileBytes, j == 0);
+        tc_commit(bar(Cfg::kBarDQDone));
+        tc_commit(bar(Cfg::kBarKVEmpty + s0));
+      }
+      if (!ok) {
+        tc_commit(bar(Cfg::kBarDrain));
+        drain_wait_b(bar(Cfg::kBarDrain), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------- elementwise
+    // Warp w owns TMEM lanes 32(w%4) + 16(w/4) .. +15; a thread holds rows
+    // lane/4 and lane/4 + 8 of that block and, of each group of 8 keys, keys
+    // 2u and 2u+1 (u = lane % 4), as the 16x256b load lays them out.
+    const int lane_base = 32 * (warp & 3) + 16 * (warp >> 2);
+    const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
+    const int u = lane & 3;
+    const int rA = lane_base + (lane >> 2);
+    const int rB = rA + 8;
+    const int iA = t * kTileRows + rA, iB = t * kTileRows + rB;       // query positions
+    const bool vA = iA < args.S, vB = iB < args.S;
+    const size_t row0 = (static_cast<size_t>(b) * args.Hq + h) * static_cast<size_t>(args.S);
+    // rows past the sequence have zero q and dO: lse2 = 0 and delta = 0 make
+    // their dS zero
+    const float lseA = vA ? __fmul_rn(args.lse[row0 + iA], kLog2e) : 0.0f;
+    const float lseB = vB ? __fmul_rn(args.lse[row0 + iB], kLog2e) : 0.0f;
+    const float dlA = vA ? args.delta[row0 + iA] : 0.0f;
+    const float dlB = vB ? args.delta[row0 + iB] : 0.0f;
+    const float c = score_scale_log2();
+    bool ok = !skip;
+    for (int j = 0; j < n_kv && ok; ++j) {
+      ok = mbar_wait(bar(Cfg::kBarSFull), j & 1, abort_flag, args.err, kDevTimeoutMma);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const bool diag = (j == n_kv - 1);
+      uint32_t ds[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sv[32], pv[32];
+        tmem_ld_16x256b_x8_wait(tmem_base + Cfg::kColS + lane_off + 64u * half, sv);
+        tmem_ld_16x256b_x8_wait(tmem_base + Cfg::kColDP + lane_off + 64u * half, pv);
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(bar(Cfg::kBarSFree));                          // S(j), dP(j) fully read
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          float dsA[2], dsB[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = 64 * half + 8 * r + 2 * u + e;           // key within the tile
+            const float pA = (diag && key > rA) ? 0.0f
+                                                : ex2_approx(__fmaf_rn(__uint_as_float(sv[4 * r + e]), c, -lseA));
+            const float pB = (diag && key > rB) ? 0.0f
+                                                : ex2_approx(__fmaf_rn(__uint_as_float(sv[4 * r + 2 + e]), c, -lseB));
+            dsA[e] = __fmul_rn(pA, __fsub_rn(__uint_as_float(pv[4 * r + e]), dlA));
+            dsB[e] = __fmul_rn(pB, __fsub_rn(__uint_as_float(pv[4 * r + 2 + e]), dlB));
+          }
+          ds[2 * (8 * half + r)] = pack_bf16x2(dsA[0], dsA[1]);
+          ds[2 * (8 * half + r) + 1] = pack_bf16x2(dsB[0], dsB[1]);
+        }
+      }
+      if (j > 0) {                                                   // dQ(j-1) has read dS(j-1)
+        ok = mbar_wait(bar(Cfg::kBarDQDone), (j - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      tmem_st_16x128b_x16(tmem_base + Cfg::kColDS + lane_off, ds);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(Cfg::kBarDSFull));
+    }
+    if (ok) ok = mbar_wait(bar(Cfg::kBarDQDone), (n_kv - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      __nv_bfloat16* base = static_cast<__nv_bfloat16*>(args.dq) + row0 * kHeadDim;
+      uint32_t* dA = reinterpret_cast<uint32_t*>(base + static_cast<size_t>(vA ? iA : 0) * kHeadDim);
+      uint32_t* dB = reinterpret_cast<uint32_t*>(base + static_cast<size_t>(vB ? iB : 0) * kHeadDim);
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[32];
+        tmem_ld_16x256b_x8_wait(tmem_base + Cfg::kColDQ + lane_off + 64u * half, v);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int col = 64 * half + 8 * r + 2 * u;
+          const uint32_t wa = pack_bf16x2(__fmul_rn(__uint_as_float(v[4 * r]), kInvSqrtD),
+                                          __fmul_rn(__uint_as_float(v[4 * r + 1]), kInvSqrtD));
+          const uint32_t wb = pack_bf16x2(__fmul_rn(__uint_as_float(v[4 * r + 2]), kInvSqrtD),
+                                          __fmul_rn(__uint_as_float(v[4 * r + 3]), kInvSqrtD));
+          if (vA) dA[col >> 1] = wa;
+          if (vB) dB[col >> 1] = wb;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == Cfg::kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------- dk/dv kernel
+
+struct BwdKVCfg {
+  static constexpr int kThreads = 320;
+  static constexpr int kLoadWarp = 8;
+  static constexpr int kMmaWarp = 9;
+  static constexpr int kStages = 2;           // Q/dO ring
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColST = 0, kColDPT = 128, kColDV = 256, kColDK = 384;
+  static constexpr uint32_t kKOff = 0;
+  static constexpr uint32_t kVOff = kTileBytes;
+  static constexpr uint32_t kQOff = 2 * kTileBytes;                   // slot s: Q at kQOff + s*2*tile,
+  static constexpr uint32_t kSlotBytes = 2 * kTileBytes;              //         dO right after it
+  static constexpr uint32_t kVecOff = kQOff + kStages * kSlotBytes;   // slot s: lse2[128], delta[128]
+  static constexpr uint32_t kVecBytes = 2 * 128 * 4;
+  static constexpr uint32_t kBarOff = kVecOff + kStages * kVecBytes;
+  static constexpr int kBarKV = 0;                                    // K(jt), V(jt) landed
+  static constexpr int kBarQDFull = 1;                                // 2: Q, dO of step s landed
+  static constexpr int kBarQDEmpty = kBarQDFull + kStages;            // 2: dV, dK of step s done
+  static constexpr int kBarVecFull = kBarQDEmpty + kStages;           // 2: lse2, delta of step s (32 arrivals)
+  static constexpr int kBarSTFull = kBarVecFull + kStages;            // S^T, dP^T of step s in TMEM
+  static constexpr int kBarPDSFull = kBarSTFull + 1;                  // P^T, dS^T stored (256 arrivals)
+  static constexpr int kBarDone = kBarPDSFull + 1;                    // every dV, dK product finished
+  static constexpr int kBarDrain = kBarDone + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
+};
+
+__global__ void __launch_bounds__(BwdKVCfg::kThreads, 1)
+kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
+                   const BwdArgs args) {
+  using Cfg = BwdKVCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_addr(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOff);
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kMiscOff);
+  volatile uint32_t* abort_flag = misc + 1;
+  auto bar = [&](int i) { return smem_addr(bars + i); };
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // (b, kv head g, key tile jt): (b, g) slowest so resident CTAs share the
+  // group's q and dO in L2; within a group the longest (jt = 0) first
+  const int bg = blockIdx.x / args.n_tiles;
+  const int jt = blockIdx.x % args.n_tiles;
+  const int b = bg / args.Hkv;
+  const int g = bg % args.Hkv;
+  const int n_q = args.n_tiles - jt;                  // query tiles jt..n-1 see this key tile
+  const int n_steps = kGroup * n_q;                   // step s: head g*4 + s / n_q, query tile jt + s % n_q
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Cfg::kNumBars; ++i) {
+      uint32_t count = 1u;
+      if (i == Cfg::kBarPDSFull) count = 256u;
+      if (i >= Cfg::kBarVecFull && i < Cfg::kBarVecFull + Cfg::kStages) count = 32u;
+      mbar_init(bar(i), count);
+    }
+    misc[1] = (*reinterpret_cast<volatile uint32_t*>(args.err) != 0) ? 1u : 0u;
+    fence_mbar_init();
+  }
+  if (warp == Cfg::kMmaWarp) {
+    tmem_alloc(sbase + Cfg::kMiscOff, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const bool skip = (*abort_flag != 0);
+
+  if (warp == Cfg::kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (!skip) {
+      const uint64_t keep = l2_policy_evict_last();
+      if (lane == 0) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_do);
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+        mbar_arrive_expect_tx(bar(Cfg::kBarKV), 2 * kTileBytes);
+        tma_load_tile(sbase + Cfg::kKOff, &tmap_k, jt * kTileRows, b * args.Hkv + g, bar(Cfg::kBarKV));
+        tma_load_tile(sbase + Cfg::kVOff, &tmap_v, jt * kTileRows, b * args.Hkv + g, bar(Cfg::kBarKV));
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int s = 0; s < n_steps; ++s) {
+        const int slot = s % Cfg::kStages;
+        const int h = g * kGroup + s / n_q;
+        const int it = jt + s % n_q;
+        if (s >= Cfg::kStages)
+          ok = mbar_wait(bar(Cfg::kBarQDEmpty + slot), ((s / Cfg::kStages) - 1) & 1, abort_flag, args.err,
+                         kDevTimeoutSlot);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const uint32_t dst = sbase + Cfg::kQOff + slot * Cfg::kSlotBytes;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(Cfg::kBarQDFull + slot), 2 * kTileBytes);
+          tma_load_tile_hint(dst, &tmap_q, it * kTileRows, b * args.Hq + h, bar(Cfg::kBarQDFull + slot), keep);
+          tma_load_tile_hint(dst + kTileBytes, &tmap_do, it * kTileRows, b * args.Hq + h,
+                             bar(Cfg::kBarQDFull + slot), keep);
+        }
+        issued = s + 1;
+        // lse (base 2) and delta of the step's 128 query rows; rows past the
+        // sequence get lse2 = +inf, so their P (and dS) is exactly zero
+        float* vec = reinterpret_cast<float*>(smem + Cfg::kVecOff + slot * Cfg::kVecBytes);
+        const size_t row0 = (static_cast<size_t>(b) * args.Hq + h) * static_cast<size_t>(args.S);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int q = 4 * lane + e;
+          const int i = it * kTileRows + q;
+          const bool valid = i < args.S;
+          vec[q] = valid ? __fmul_rn(args.lse[row0 + i], kLog2e) : __int_as_float(0x7F800000);
+          vec[128 + q] = valid ? args.delta[row0 + i] : 0.0f;
+        }
+        mbar_arrive(bar(Cfg::kBarVecFull + slot));
+      }
+      if (!ok && lane == 0) {
+        drain_wait_b(bar(Cfg::kBarKV), 0);
+        for (int x = (issued > Cfg::kStages ? issued - Cfg::kStages : 0); x < issued; ++x)
+          drain_wait_b(bar(Cfg::kBarQDFull + x % Cfg::kStages), (x / Cfg::kStages) & 1);
+      }
+    }
+  } else if (warp == Cfg::kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    // per step: S^T = K Q^T, dP^T = V dO^T | (P^T, dS^T stored) dV += P^T dO,
+    // dK += dS^T Q.  P^T and dS^T overwrite S^T and dP^T, whose next values
+    // are issued after these products (in issue order).
+    if (lane == 0 && !skip) {
+      bool ok = mbar_wait(bar(Cfg::kBarKV), 0, abort_flag, args.err, kDevTimeoutTma);
+      for (int s = 0; s < n_steps && ok; ++s) {
+        const int slot = s % Cfg::kStages;
+        const uint32_t q_s = sbase + Cfg::kQOff + slot * Cfg::kSlotBytes;
+        const uint32_t do_s = q_s + kTileBytes;
+        ok = mbar_wait(bar(Cfg::kBarQDFull + slot), (s / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+        if (!ok) break;
+        tc_fence_after();
+        issue_qk(tmem_base + Cfg::kColST, sbase + Cfg::kKOff, 1024u, kSlabBytes, q_s);
+        issue_qk(tmem_base + Cfg::kColDPT, sbase + Cfg::kVOff, 1024u, kSlabBytes, do_s);
+        tc_commit(bar(Cfg::kBarSTFull));
+        ok = mbar_wait(bar(Cfg::kBarPDSFull), s & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, s == 0);
+        issue_pv(tmem_base + Cfg::kColDK, tmem_base + Cfg::kColDPT, q_s, s == 0);
+        tc_commit(bar(Cfg::kBarQDEmpty + slot));
+      }
+      if (ok) tc_commit(bar(Cfg::kBarDone));
+      if (!ok) {
+        tc_commit(bar(Cfg::kBarDrain));
+        drain_wait_b(bar(Cfg::kBarDrain), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------- elementwise
+    // rows are keys (lanes as in the dq kernel), columns are query rows
+    const int lane_base = 32 * (warp & 3) + 16 * (warp >> 2);
+    const uint32_t lane_off = static_cast<uint32_t>(lane_base) << 16;
+    const int u = lane & 3;
+    const int rA = lane_base + (lane >> 2);
+    const int rB = rA + 8;
+    const float c = score_scale_log2();
+    bool ok = !skip;
+    for (int s = 0; s < n_steps && ok; ++s) {
+      const int slot = s % Cfg::kStages;
+      const bool diag = (s % n_q) == 0;                              // query tile jt: keys past the row masked
+      ok = mbar_wait(bar(Cfg::kBarSTFull), s & 1, abort_flag, args.err, kDevTimeoutMma);
+      if (ok) ok = mbar_wait(bar(Cfg::kBarVecFull + slot), (s / Cfg::kStages) & 1, abort_flag, args.err,
+                             kDevTimeoutTma);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float* vlse = reinterpret_cast<const float*>(smem + Cfg::kVecOff + slot * Cfg::kVecBytes);
+      const float* vdl = vlse + 128;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sv[32], pv[32];
+        tmem_ld_16x256b_x8_wait(tmem_base + Cfg::kColST + lane_off + 64u * half, sv);
+        tmem_ld_16x256b_x8_wait(tmem_base + Cfg::kColDPT + lane_off + 64u * half, pv);
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          float pA[2], pB[2], dA[2], dB[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int qc = 64 * half + 8 * r + 2 * u + e;            // query row within its tile
+            const float l2 = vlse[qc];
+            const float dl = vdl[qc];
+            pA[e] = (diag && rA > qc) ? 0.0f : ex2_approx(__fmaf_rn(__uint_as_float(sv[4 * r + e]), c, -l2));
+            pB[e] = (diag && rB > qc) ? 0.0f : ex2_approx(__fmaf_rn(__uint_as_float(sv[4 * r + 2 + e]), c, -l2));
+            dA[e] = __fmul_rn(pA[e], __fsub_rn(__uint_as_float(pv[4 * r + e]), dl));
+            dB[e] = __fmul_rn(pB[e], __fsub_rn(__uint_as_float(pv[4 * r + 2 + e]), dl));
+          }
+          pp[2 * r] = pack_bf16x2(pA[0], pA[1]);
+          pp[2 * r + 1] = pack_bf16x2(pB[0], pB[1]);
+          dd[2 * r] = pack_bf16x2(dA[0], dA[1]);
+          dd[2 * r + 1] = pack_bf16x2(dB[0], dB[1]);
+        }
+        // bf16 pairs of query columns 64*half.. go to columns 32*half.. of the
+        // same buffers; those fp32 columns were read in half 0
+        tmem_st_16x128b_x8(tmem_base + Cfg::kColST + lane_off + 32u * half, pp);
+        tmem_st_16x128b_x8(tmem_base + Cfg::kColDPT + lane_off + 32u * half, dd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(Cfg::kBarPDSFull));
+    }
+    if (ok) ok = mbar_wait(bar(Cfg::kBarDone), 0, abort_flag, args.err, kDevTimeoutMma);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      const int jA = jt * kTileRows + rA, jB = jt * kTileRows + rB;
+      const bool vA = jA < args.S, vB = jB < args.S;
+      const size_t kv0 = (static_cast<size_t>(b) * args.Hkv + g) * static_cast<size_t>(args.S);
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {                      // 0: dv, 1: dk (scaled by 1/sqrt(128))
+        __nv_bfloat16* base = static_cast<__nv_bfloat16*>(which ? args.dk : args.dv) + kv0 * kHeadDim;
+        uint32_t* oA = reinterpret_cast<uint32_t*>(base + static_cast<size_t>(vA ? jA : 0) * kHeadDim);
+        uint32_t* oB = reinterpret_cast<uint32_t*>(base + static_cast<size_t>(vB ? jB : 0) * kHeadDim);
+        const float sc = which ? kInvSqrtD : 1.0f;
+        const uint32_t col0 = which ? Cfg::kColDK : Cfg::kColDV;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+          tmem_ld_16x256b_x8_wait(tmem_base + col0 + lane_off + 64u * half, v);
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const int col = 64 * half + 8 * r + 2 * u;
+            const uint32_t wa = pack_bf16x2(__fmul_rn(__uint_as_float(v[4 * r]), sc),
+                                            __fmul_rn(__uint_as_float(v[4 * r + 1]), sc));
+            const uint32_t wb = pack_bf16x2(__fmul_rn(__uint_as_float(v[4 * r + 2]), sc),
+                                            __fmul_rn(__uint_as_float(v[4 * r + 3]), sc));
+            if (vA) oA[col >> 1] = wa;
+            if (vB) oB[col >> 1] = wb;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == Cfg::kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// --------------------------------------------------------------- launcher
+
+cudaError_t launch_backward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t s) {
+  static_assert(BwdQCfg::kSmemBytes <= 227u * 1024u, "shared memory budget (dq)");
+  static_assert(BwdKVCfg::kSmemBytes <= 227u * 1024u, "shared memory budget (dk, dv)");
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(kb_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(BwdQCfg::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kb_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(BwdKVCfg::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const long long rows = static_cast<long long>(a.B) * a.Hq * a.S;
+  kb_bwd_delta_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.delta, rows);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long grid_q = static_cast<long long>(a.n_tiles) * a.B * a.Hq;
+  kb_bwd_dq_kernel<<<static_cast<unsigned>(grid_q), BwdQCfg::kThreads, BwdQCfg::kSmemBytes, s>>>(tq, tk, tv, tdo, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long grid_kv = static_cast<long long>(a.n_tiles) * a.B * a.Hkv;
+  kb_bwd_dkdv_kernel<<<static_cast<unsigned>(grid_kv), BwdKVCfg::kThreads, BwdKVCfg::kSmemBytes, s>>>(tq, tk, tv,
+                                                                                                     tdo, a);
+  return cudaGetLastError();
+}
+
+}  // namespace kb

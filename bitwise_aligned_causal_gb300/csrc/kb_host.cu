@@ -135,7 +135,7 @@ struct Ragged {
 
 kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int L, int start,
                      int kv_cap, int q_tiles_per_cta, void* stream, const Paging* paging = nullptr,
-                     const Ragged* ragged = nullptr) {
+                     const Ragged* ragged = nullptr, float* lse = nullptr) {
   kb_status s = check_ptrs(q, k, v, o);
   if (s != KB_OK) return s;
   if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
@@ -144,6 +144,7 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   if (kv_cap > kMaxRows) return KB_ERR_UNSUPPORTED;
   if (q_tiles_per_cta < 0 || q_tiles_per_cta > kb::kShapeOneTilePerSm) return KB_ERR_INVALID_ARG;
   if (q_tiles_per_cta == 0 && L > kb::kMaxPackedRows) return KB_ERR_INVALID_ARG;
+  if (lse != nullptr && q_tiles_per_cta != kb::kShapeOneTilePerSm) return KB_ERR_INVALID_ARG;
   // a ragged batch sizes the grid for its longest possible sequence
   const int first_tile = ragged ? 0 : start / kb::kTileRows;
   const int last_tile = ragged ? (L + kb::kTileRows - 2) / kb::kTileRows : (start + L - 1) / kb::kTileRows;
@@ -160,6 +161,7 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   for (const void* p : {q, k, v, static_cast<const void*>(o)})
     if ((s = check_device_pointer(p)) != KB_OK) return s;
   if (paging && (s = check_device_pointer(paging->block_table)) != KB_OK) return s;
+  if (lse && (s = check_device_pointer(lse)) != KB_OK) return s;
   if (ragged) {
     if ((s = check_device_pointer(ragged->starts)) != KB_OK) return s;
     if ((s = check_device_pointer(ragged->lens)) != KB_OK) return s;
@@ -224,6 +226,7 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   // beyond a few waves, order CTAs by GQA group so that the resident ones
   // share K/V in L2; below that, globally longest tile first
   a.group_major = grid > 4LL * dst->sm_count ? 1 : 0;
+  a.lse = lse;
   if (ragged) {
     a.starts = ragged->starts;
     a.lens = ragged->lens;
@@ -265,6 +268,58 @@ kb_status kb_attn_prefill(const void* q, const void* k, const void* v, void* o, 
                           void* stream) {
   if (S < 1) return KB_ERR_INVALID_ARG;
   return chunk_impl(q, k, v, o, B, Hq, Hkv, S, 0, S, chunk_cta_shape(S), stream);
+}
+
+kb_status kb_attn_prefill_lse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                              int Hkv, int S, void* stream) {
+  if (S < 1 || lse == nullptr) return KB_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return KB_ERR_INVALID_ARG;
+  return chunk_impl(q, k, v, o, B, Hq, Hkv, S, 0, S, kb::kShapeOneTilePerSm, stream, nullptr, nullptr, lse);
+}
+
+kb_status kb_attn_backward(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                           const float* lse, float* delta, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+                           int S, void* stream) {
+  kb_status s = check_ptrs(q, k, v, o);
+  if (s != KB_OK) return s;
+  if ((s = check_ptrs(dout, dq, dk, dv)) != KB_OK) return s;
+  if (!lse || !delta || (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(delta) & 3u))
+    return KB_ERR_INVALID_ARG;
+  if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
+  if (S < 1) return KB_ERR_INVALID_ARG;
+  if (S > kMaxRows) return KB_ERR_UNSUPPORTED;
+  const int n_tiles = (S + kb::kTileRows - 1) / kb::kTileRows;
+  if (static_cast<long long>(n_tiles) * B * Hq > 0x7FFFFFFFLL) return KB_ERR_UNSUPPORTED;
+  DeviceState* dst = nullptr;
+  if ((s = get_device_state(&dst)) != KB_OK) return s;
+  for (const void* p : {q, k, v, o, dout, static_cast<const void*>(lse), static_cast<const void*>(delta),
+                        static_cast<const void*>(dq), static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    if ((s = check_device_pointer(p)) != KB_OK) return s;
+  CUtensorMap tq, tk, tv, tdo;
+  const uint64_t row_bytes = kb::kHeadDim * 2u;
+  const uint64_t rows = static_cast<uint64_t>(S);
+  if ((s = encode_rows_map(&tq, q, rows, static_cast<uint64_t>(B) * Hq, rows * row_bytes)) != KB_OK) return s;
+  if ((s = encode_rows_map(&tdo, dout, rows, static_cast<uint64_t>(B) * Hq, rows * row_bytes)) != KB_OK) return s;
+  if ((s = encode_rows_map(&tk, k, rows, static_cast<uint64_t>(B) * Hkv, rows * row_bytes)) != KB_OK) return s;
+  if ((s = encode_rows_map(&tv, v, rows, static_cast<uint64_t>(B) * Hkv, rows * row_bytes)) != KB_OK) return s;
+  kb::BwdArgs a{};
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.delta = delta;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.S = S;
+  a.n_tiles = n_tiles;
+  a.group_major = static_cast<long long>(n_tiles) * B * Hq > 4LL * dst->sm_count ? 1 : 0;
+  a.err = dst->err;
+  const cudaError_t e = kb::launch_backward(tq, tk, tv, tdo, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return KB_OK;
 }
 
 kb_status kb_attn_chunk_paged(const void* q, const void* k_pages, const void* v_pages, void* o, int B, int Hq,

@@ -21,6 +21,7 @@ struct PrefillArgs {
   const int* lens;         //   L is the row stride of q and o and lens[b] <= L rows are used)
   int kv_cap;              // keys per sequence the cache can hold
   int group_major;         // CTA order: 1 = (b, g) slowest, 0 = query tile slowest
+  float* lse;              // optional [B, Hq, L] fp32: natural-log log-sum-exp of each row's scaled scores
   uint32_t* err;    // device error word
 };
 
@@ -55,6 +56,24 @@ cudaError_t launch_prefill_s2(const CUtensorMap& tq, const CUtensorMap& tk, cons
 // n_sub: 1, or 2 when the chunk crosses a 128-position tile boundary.
 cudaError_t launch_packed(const CUtensorMap& tk, const CUtensorMap& tv, const PackedArgs& a, int n_sub,
                           cudaStream_t s);
+// Gradient of a whole-sequence causal prefill (query row i at position i).
+struct BwdArgs {
+  const void* o;           // [B, Hq, S, 128] bf16 forward output
+  const void* dout;        // [B, Hq, S, 128] bf16 gradient of the output
+  const float* lse;        // [B, Hq, S] natural-log log-sum-exp from the forward
+  float* delta;            // [B, Hq, S] out: rowsum(dout * o)
+  void* dq;                // [B, Hq, S, 128] bf16 out
+  void* dk;                // [B, Hkv, S, 128] bf16 out
+  void* dv;                // [B, Hkv, S, 128] bf16 out
+  int B, Hq, Hkv, S;
+  int n_tiles;             // ceil(S / 128)
+  int group_major;         // CTA order of the dq kernel (as PrefillArgs)
+  uint32_t* err;
+};
+// delta, then dq (query-major), then dk/dv (key-major), all on stream s.
+// tq, tdo: [B*Hq planes, S rows]; tk, tv: [B*Hkv planes, S rows].
+cudaError_t launch_backward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_wait_probe(uint32_t* err, unsigned long long limit_ns, cudaStream_t s);
 
 }  // namespace kb

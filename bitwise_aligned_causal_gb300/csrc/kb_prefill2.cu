@@ -345,6 +345,14 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       const int iB = iA + 8;
       const bool stA = (iA >= 0) && (iA < L);
       const bool stB = (iB >= 0) && (iB < L);
+      if (args.lse != nullptr && u == 0) {
+        // natural-log log-sum-exp of the row's scaled scores: the weights are
+        // 2^(s c - mc), so log2 sum_j 2^(s_j c) = mc + log2(l)
+        constexpr float kLn2 = 0.69314718055994531f;
+        float* lrow = args.lse + (static_cast<size_t>(b) * args.Hq + h) * static_cast<size_t>(args.L);
+        if (stA) lrow[iA] = __fmul_rn(__fadd_rn(sA.mc, log2f(sA.l)), kLn2);
+        if (stB) lrow[iB] = __fmul_rn(__fadd_rn(sB.mc, log2f(sB.l)), kLn2);
+      }
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.o) + (static_cast<size_t>(b) * args.Hq + h) *
                                                                        static_cast<size_t>(args.L) * kHeadDim;
       uint32_t* dA = reinterpret_cast<uint32_t*>(orow + static_cast<size_t>(stA ? iA : 0) * kHeadDim);

@@ -360,6 +360,18 @@ __device__ __forceinline__ void tmem_st_16x128b_x16(uint32_t taddr, const uint32
 }
 #undef KB_V8
 
+// 16x128b shape, 8 repetitions: columns 0..31 of the same layout as above.
+#define KB_V8(b) "r"(v[b + 0]), "r"(v[b + 1]), "r"(v[b + 2]), "r"(v[b + 3]), \
+                 "r"(v[b + 4]), "r"(v[b + 5]), "r"(v[b + 6]), "r"(v[b + 7])
+__device__ __forceinline__ void tmem_st_16x128b_x8(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x8.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), KB_V8(0), KB_V8(8)
+      : "memory");
+}
+#undef KB_V8
+
 // ---------------------------------------------------------------- arithmetic
 
 __device__ __forceinline__ float ex2_approx(float x) {

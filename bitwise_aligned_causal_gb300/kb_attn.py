@@ -39,6 +39,8 @@ _SIGS = {
     "kb_attn_check_device_status": [_P],
     "kb_attn_debug_wait_timeout": [_I, _P],
     "kb_attn_chunk_cta_shape": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P],
+    "kb_attn_prefill_lse": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P],
+    "kb_attn_backward": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P],
     "kb_status_string": [_I],
     "kb_contract_version": [],
     "kb_attn_last_cuda_error": [],
@@ -111,6 +113,14 @@ def kb_attn_chunk_varlen(q, k, v, o, B, Hq, Hkv, L_max, starts, lens, kv_cap, bl
 
 def kb_attn_chunk_cta_shape(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, q_tiles_per_cta, stream=None) -> int:
     return _lib.kb_attn_chunk_cta_shape(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, q_tiles_per_cta, stream)
+
+
+def kb_attn_prefill_lse(q, k, v, o, lse, B, Hq, Hkv, S, stream=None) -> int:
+    return _lib.kb_attn_prefill_lse(q, k, v, o, lse, B, Hq, Hkv, S, stream)
+
+
+def kb_attn_backward(q, k, v, o, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, stream=None) -> int:
+    return _lib.kb_attn_backward(q, k, v, o, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, stream)
 
 
 def kb_attn_check_device_status(stream=None) -> int:
@@ -261,3 +271,50 @@ def chunk_varlen(q, k, v, starts, lens, out=None, block_table=None, stream=None)
 
 def check_device_status(stream=None):
     _raise(kb_attn_check_device_status(_stream(stream)), "kb_attn_check_device_status")
+
+
+def _check_f32(t, name, shape):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous float32 CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}")
+
+
+def prefill_lse(q, k, v, out=None, lse=None, stream=None):
+    """Training forward: (o, lse) with o bit-identical to prefill and lse [B,Hq,S] float32 the
+    natural-log log-sum-exp of each row's scaled scores."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, 4)
+    B, Hq, S, _ = q.shape
+    Hkv = k.shape[1]
+    o = torch.empty_like(q) if out is None else out
+    _check(o, "out", 4)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_f32(lse, "lse", (B, Hq, S))
+    _raise(kb_attn_prefill_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv,
+                               S, _stream(stream)), "kb_attn_prefill_lse")
+    return o, lse
+
+
+def backward(q, k, v, o, dout, lse, delta=None, dq=None, dk=None, dv=None, stream=None):
+    """Gradients (dq, dk, dv) of the whole-sequence causal prefill for output gradient dout; o and
+    lse from prefill_lse.  Also returns delta [B,Hq,S] float32 = rowsum(dout * o)."""
+    torch = _torch()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _check(t, n, 4)
+    B, Hq, S, _ = q.shape
+    Hkv = k.shape[1]
+    _check_f32(lse, "lse", (B, Hq, S))
+    delta = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if delta is None else delta
+    _check_f32(delta, "delta", (B, Hq, S))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, 4)
+    _raise(kb_attn_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                            delta.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, S,
+                            _stream(stream)), "kb_attn_backward")
+    return dq, dk, dv, delta

@@ -158,6 +158,42 @@ kb_status kb_attn_check_device_status(void* stream);
 kb_status kb_attn_debug_wait_timeout(int limit_us, void* stream);
 
 /*
+ * Training forward: kb_attn_prefill plus each row's log-sum-exp, which the
+ * backward needs (README "Motivation": the RL policy update differentiates
+ * the same attention).
+ *   q, o, k, v : as kb_attn_prefill; o gets the same bits as kb_attn_prefill
+ *   lse        : [B, Hq, S] fp32, device, 4-byte aligned, caller-owned;
+ *                lse[b,h,i] = ln sum_{j<=i} exp(q_i . k_j / sqrt(128))
+ * Always runs the one-query-tile-per-CTA kernel (CTA shape 3), whose bits
+ * every other shape reproduces.
+ */
+kb_status kb_attn_prefill_lse(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int Hq, int Hkv, int S, void* stream);
+
+/*
+ * Backward of the whole-sequence causal prefill (query row i at position i):
+ * the gradients of q, k and v for a given gradient dout of the output.
+ *   q, dout, o : [B, Hq, S, 128] bf16; o and lse from kb_attn_prefill_lse
+ *   k, v       : [B, Hkv, S, 128] bf16
+ *   lse        : [B, Hq, S] fp32 (input)
+ *   delta      : [B, Hq, S] fp32 (output): delta[b,h,i] = dout_i . o_i
+ *   dq         : [B, Hq, S, 128] bf16 (output)
+ *   dk, dv     : [B, Hkv, S, 128] bf16 (output); each sums the four query
+ *                heads of its group
+ * With P the softmax rows recomputed from lse, dP_ij = dout_i . v_j and
+ * dS_ij = P_ij (dP_ij - delta_i):
+ *   dq_i = sum_j dS_ij k_j / sqrt(128),  dk_j = sum_{h,i} dS_ij q_i / sqrt(128),
+ *   dv_j = sum_{h,i} P_ij dout_i   (P and dS rounded to bf16 for the products,
+ *   fp32 accumulation, bf16 outputs).
+ * No atomics: every output element is summed by one CTA in a fixed order, so
+ * repeated calls give identical bits.  All pointers are device memory,
+ * caller-owned; errors as for the forward entry points.
+ */
+kb_status kb_attn_backward(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                           const float* lse, float* delta, void* dq, void* dk, void* dv,
+                           int B, int Hq, int Hkv, int S, void* stream);
+
+/*
  * Prefill/chunk with an explicit kernel shape, for tests of the contract:
  * q_tiles_per_cta = 1 or 2 runs the tile kernel with that many 128-row query
  * tiles per CTA; 3 runs the tile kernel with one query tile per CTA, one CTA

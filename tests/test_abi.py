@@ -91,6 +91,22 @@ def test_paged_decode_arguments_rejected(kb):
     assert kb.kb_attn_decode_paged(FAKE, FAKE, FAKE, FAKE, 2, 32, 4, FAKE, 4, 128, 10, FAKE) == kb.KB_ERR_UNSUPPORTED
 
 
+def test_training_entry_points_reject_bad_arguments(kb):
+    args = (FAKE, FAKE, FAKE, FAKE)
+    assert kb.kb_attn_prefill_lse(*args, None, 1, 32, 8, 64) == kb.KB_ERR_INVALID_ARG       # no lse
+    assert kb.kb_attn_prefill_lse(*args, FAKE + 2, 1, 32, 8, 64) == kb.KB_ERR_INVALID_ARG   # misaligned lse
+    assert kb.kb_attn_prefill_lse(*args, FAKE, 1, 32, 8, 0) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_prefill_lse(*args, FAKE, 1, 32, 4, 64) == kb.KB_ERR_UNSUPPORTED       # Hq != 4 Hkv
+    ok = (FAKE, FAKE, FAKE, FAKE, FAKE)                                                     # q k v o dout
+    outs = (FAKE, FAKE, FAKE)                                                               # dq dk dv
+    assert kb.kb_attn_backward(*ok, None, FAKE, *outs, 1, 32, 8, 64) == kb.KB_ERR_INVALID_ARG   # no lse
+    assert kb.kb_attn_backward(*ok, FAKE, None, *outs, 1, 32, 8, 64) == kb.KB_ERR_INVALID_ARG   # no delta
+    assert kb.kb_attn_backward(*ok, FAKE, FAKE, FAKE + 8, FAKE, FAKE, 1, 32, 8, 64) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_backward(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, *outs, 1, 32, 8, 64) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_backward(*ok, FAKE, FAKE, *outs, 1, 32, 8, 0) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_backward(*ok, FAKE, FAKE, *outs, 1, 32, 2, 64) == kb.KB_ERR_UNSUPPORTED
+
+
 def test_packed_shape_limits(kb):
     assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 33, 0, 64, 0) == kb.KB_ERR_INVALID_ARG
     assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 4, 0, 64, -1) == kb.KB_ERR_INVALID_ARG
