@@ -36,6 +36,7 @@ WORKLOADS = {"full": (4, 16384, 16, 8192), "small": (4, 4096, 16, 8192)}
 PREFILL_B, PREFILL_S, DECODE_B, DECODE_CTX = WORKLOADS["full"]
 SEED_PREFILL = 7_000_001
 SEED_DECODE = 7_000_002
+SEED_BACKWARD = 7_000_003
 
 
 def workload_name():
@@ -300,9 +301,47 @@ def run_ours(args, rank, world, local):
         e2e = None
     else:
         e2e = run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_attn)
+    bwd = None if args.no_backward else run_backward(args, q, k, v, stream, world, local, rank, kb_attn)
     if rank != 0:
         return
-    emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks, x)
+    emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks, x,
+              bwd)
+
+
+def run_backward(args, q, k, v, stream, world, local, rank, kb_attn):
+    """The training pair on the prefill workload: kb_attn_prefill_lse, then
+    kb_attn_backward for a seeded N(0,1) output gradient, each timed alone
+    (CUDA events on the launching stream, device-resident inputs)."""
+    import numpy as np
+    import torch
+
+    from bitwise_aligned_causal_gb300 import inputs
+
+    dob = inputs.make_qkv(PREFILL_B, PREFILL_S, SEED_BACKWARD + 1000 * rank).q
+    do = torch.from_numpy(np.ascontiguousarray(dob).view(np.int16)).view(torch.bfloat16).to(q.device)
+    o, lse = kb_attn.prefill_lse(q, k, v)
+    dq, dk, dv, delta = kb_attn.backward(q, k, v, o, do, lse)
+    reps = max(3, min(args.steps, 10))
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    barrier(world, local)
+    fwd_ms = timed(lambda: kb_attn.prefill_lse(q, k, v, out=o, lse=lse))
+    bwd_ms = timed(lambda: kb_attn.backward(q, k, v, o, do, lse, delta=delta, dq=dq, dk=dk, dv=dv))
+    kb_attn.check_device_status()
+    dev = "cuda" if world > 1 else "cpu"
+    return {"fwd_ms": reduce_max(fwd_ms, world, dev), "bwd_ms": reduce_max(bwd_ms, world, dev), "reps": reps,
+            "fwd_ms_local": fwd_ms, "bwd_ms_local": bwd_ms}
 
 
 def pipelined_e2e(n, host_in, dev_sets, host_out, launch):
@@ -408,7 +447,7 @@ def run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_att
 
 
 def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks,
-              x):
+              x, bwd=None):
     pf = prefill_flops(PREFILL_B, PREFILL_S)
     db = decode_bytes(DECODE_B, DECODE_CTX)
     peaks = load_peaks()
@@ -460,6 +499,21 @@ def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_ma
         "gpu_launches": 2 * n,
         "clocks": clocks,
     }
+    if bwd is not None:
+        bf = 2.5 * pf                                   # dq, dk, dv: five products of the forward's size
+        per_launch = bf / (bwd["bwd_ms_local"] / 1e3) / 1e12
+        line["backward"] = {
+            "value": 2.5 * aggregate(pf, world, bwd["bwd_ms"] / 1e3) / 1e12, "unit": "TFLOP/s", "ms": bwd["bwd_ms"],
+            "flops": "algorithmic 2.5 x the forward's (five products over the visible pairs)",
+            "workload": f"kb_attn_backward on the prefill workload (B={PREFILL_B} S={PREFILL_S}), dO ~ N(0,1)",
+            "forward_with_lse": {"value": aggregate(pf, world, bwd["fwd_ms"] / 1e3) / 1e12, "unit": "TFLOP/s",
+                                 "ms": bwd["fwd_ms"]},
+            "reps": bwd["reps"],
+            "roofline": {"bound": "tensor", "achieved": per_launch, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": per_launch / peaks["bf16_tflops"], "traffic": None,
+                         "kernel": "kb_bwd_delta_kernel + kb_bwd_dq_kernel + kb_bwd_dkdv_kernel (one call)",
+                         "peak_source": peaks["source"] + " burst bf16"},
+        }
     print(json.dumps(line), flush=True)
 
 
@@ -530,6 +584,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip timing the training forward + backward")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="full")
     ap.add_argument("--sweep", action="store_true",
                     help="time every prefill (S x B) and decode (ctx x B) configuration of the grid instead")

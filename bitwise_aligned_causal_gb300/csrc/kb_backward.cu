@@ -38,6 +38,30 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
     if (global_timer_ns() - t0 > 50000000ull) break;
 }
 
+// Two independent products of the same shape, their K steps interleaved
+// (each accumulator still takes its eight steps in ascending order): the
+// tensor pipe overlaps the two dependency chains.
+__device__ __forceinline__ void issue_qk_pair(uint32_t d1, uint32_t a1, uint32_t b1, uint32_t d2, uint32_t a2,
+                                              uint32_t b2) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    mma_ss(d1, desc_kmajor(a1, kk, 1024u, kSlabBytes), desc_kmajor(b1, kk, 1024u, kSlabBytes), kIdescQK,
+           kk > 0 ? 1u : 0u);
+    mma_ss(d2, desc_kmajor(a2, kk, 1024u, kSlabBytes), desc_kmajor(b2, kk, 1024u, kSlabBytes), kIdescQK,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void issue_pv_pair(uint32_t d1, uint32_t a1_tmem, uint32_t b1, uint32_t d2,
+                                              uint32_t a2_tmem, uint32_t b2, bool first) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+    mma_ts(d1, a1_tmem + static_cast<uint32_t>(kk) * 8u, desc_v(b1, kk), kIdescPV, acc);
+    mma_ts(d2, a2_tmem + static_cast<uint32_t>(kk) * 8u, desc_v(b2, kk), kIdescPV, acc);
+  }
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -66,9 +90,10 @@ __global__ void __launch_bounds__(256) kb_bwd_delta_kernel(const __nv_bfloat16* 
 // -------------------------------------------------------------- dq kernel
 
 struct BwdQCfg {
-  static constexpr int kThreads = 320;        // 8 elementwise warps, producer, MMA issuer
+  static constexpr int kThreads = 352;        // 8 elementwise warps, producer, two MMA issuers
   static constexpr int kLoadWarp = 8;
-  static constexpr int kMmaWarp = 9;
+  static constexpr int kMmaWarp = 9;          // TMEM allocator + S, dP issuer
+  static constexpr int kDqWarp = 10;          // dQ issuer
   static constexpr int kStages = 2;           // K/V ring
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;
@@ -84,8 +109,8 @@ struct BwdQCfg {
   static constexpr int kBarSFree = kBarSFull + 1;          // S(j), dP(j) read (256 arrivals)
   static constexpr int kBarDSFull = kBarSFree + 1;         // dS(j) in TMEM (256 arrivals)
   static constexpr int kBarDQDone = kBarDSFull + 1;        // dQ += dS(j) K(j) finished
-  static constexpr int kBarDrain = kBarDQDone + 1;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarDrain = kBarDQDone + 1;          // 2: one per issuer
+  static constexpr int kNumBars = kBarDrain + 2;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -179,42 +204,46 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       }
     }
   } else if (warp == Cfg::kMmaWarp) {
-    // ---------------------------------------------------------- MMA issuer
-    // S(0) dP(0) | S(1) dP(1) [after S(0), dP(0) were read] dQ(0) [after
-    // dS(0)] | S(2) dP(2) dQ(1) | ...  dQ(j) reads K(j) and dS(j) only.
+    // ------------------------------------------------------ S, dP issuer
+    // S(j+1), dP(j+1) go out as soon as the elementwise warps have read S(j),
+    // dP(j); a second thread issues the dQ products, so neither stream's
+    // barrier waits leave the tensor pipe idle.
     if (lane == 0 && !skip) {
       const uint32_t q_s = sbase + Cfg::kQOff, do_s = sbase + Cfg::kDOOff;
       bool ok = mbar_wait(bar(Cfg::kBarQD), 0, abort_flag, args.err, kDevTimeoutTma);
-      if (ok) ok = mbar_wait(bar(Cfg::kBarKVFull), 0, abort_flag, args.err, kDevTimeoutTma);
-      if (ok) {
-        tc_fence_after();
-        issue_qk(tmem_base + Cfg::kColS, q_s, 1024u, kSlabBytes, sbase + Cfg::kKOff);
-        issue_qk(tmem_base + Cfg::kColDP, do_s, 1024u, kSlabBytes, sbase + Cfg::kVOff);
-        tc_commit(bar(Cfg::kBarSFull));
-      }
       for (int j = 0; j < n_kv && ok; ++j) {
-        if (j + 1 < n_kv) {
-          const int s1 = (j + 1) % Cfg::kStages;
-          ok = mbar_wait(bar(Cfg::kBarKVFull + s1), ((j + 1) / Cfg::kStages) & 1, abort_flag, args.err,
-                         kDevTimeoutTma);
-          if (ok) ok = mbar_wait(bar(Cfg::kBarSFree), j & 1, abort_flag, args.err, kDevTimeoutSoftmax);
-          if (!ok) break;
-          tc_fence_after();
-          issue_qk(tmem_base + Cfg::kColS, q_s, 1024u, kSlabBytes, sbase + Cfg::kKOff + s1 * kTileBytes);
-          issue_qk(tmem_base + Cfg::kColDP, do_s, 1024u, kSlabBytes, sbase + Cfg::kVOff + s1 * kTileBytes);
-          tc_commit(bar(Cfg::kBarSFull));
-        }
-        ok = mbar_wait(bar(Cfg::kBarDSFull), j & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        const int slot = j % Cfg::kStages;
+        ok = mbar_wait(bar(Cfg::kBarKVFull + slot), (j / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+        if (ok && j > 0) ok = mbar_wait(bar(Cfg::kBarSFree), (j - 1) & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
-        const int s0 = j % Cfg::kStages;
-        issue_pv(tmem_base + Cfg::kColDQ, tmem_base + Cfg::kColDS, sbase + Cfg::kKOff + s0 * kTileBytes, j == 0);
-        tc_commit(bar(Cfg::kBarDQDone));
-        tc_commit(bar(Cfg::kBarKVEmpty + s0));
+        issue_qk_pair(tmem_base + Cfg::kColS, q_s, sbase + Cfg::kKOff + slot * kTileBytes,
+                      tmem_base + Cfg::kColDP, do_s, sbase + Cfg::kVOff + slot * kTileBytes);
+        tc_commit(bar(Cfg::kBarSFull));
       }
       if (!ok) {
         tc_commit(bar(Cfg::kBarDrain));
         drain_wait_b(bar(Cfg::kBarDrain), 0);
+      }
+    }
+  } else if (warp == Cfg::kDqWarp) {
+    // ---------------------------------------------------------- dQ issuer
+    // dQ(j) reads dS(j) and K(j); the K/V slot is released after it (S(j) and
+    // dP(j) finished before dS(j) existed).
+    if (lane == 0 && !skip) {
+      bool ok = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        ok = mbar_wait(bar(Cfg::kBarDSFull), j & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        if (!ok) break;
+        tc_fence_after();
+        const int slot = j % Cfg::kStages;
+        issue_pv(tmem_base + Cfg::kColDQ, tmem_base + Cfg::kColDS, sbase + Cfg::kKOff + slot * kTileBytes, j == 0);
+        tc_commit(bar(Cfg::kBarDQDone));
+        tc_commit(bar(Cfg::kBarKVEmpty + slot));
+      }
+      if (!ok) {
+        tc_commit(bar(Cfg::kBarDrain + 1));
+        drain_wait_b(bar(Cfg::kBarDrain + 1), 0);
       }
     }
   } else {
@@ -455,14 +484,14 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         ok = mbar_wait(bar(Cfg::kBarQDFull + slot), (s / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
         if (!ok) break;
         tc_fence_after();
-        issue_qk(tmem_base + Cfg::kColST, sbase + Cfg::kKOff, 1024u, kSlabBytes, q_s);
-        issue_qk(tmem_base + Cfg::kColDPT, sbase + Cfg::kVOff, 1024u, kSlabBytes, do_s);
+        issue_qk_pair(tmem_base + Cfg::kColST, sbase + Cfg::kKOff, q_s, tmem_base + Cfg::kColDPT, sbase + Cfg::kVOff,
+                      do_s);
         tc_commit(bar(Cfg::kBarSTFull));
         ok = mbar_wait(bar(Cfg::kBarPDSFull), s & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
-        issue_pv(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, s == 0);
-        issue_pv(tmem_base + Cfg::kColDK, tmem_base + Cfg::kColDPT, q_s, s == 0);
+        issue_pv_pair(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, tmem_base + Cfg::kColDK,
+                      tmem_base + Cfg::kColDPT, q_s, s == 0);
         tc_commit(bar(Cfg::kBarQDEmpty + slot));
       }
       if (ok) tc_commit(bar(Cfg::kBarDone));
