@@ -52,10 +52,11 @@ __device__ __forceinline__ void issue_qk_pair(uint32_t d1, uint32_t a1, uint32_t
   }
 }
 
+template <int kFrom, int kTo>
 __device__ __forceinline__ void issue_pv_pair(uint32_t d1, uint32_t a1_tmem, uint32_t b1, uint32_t d2,
                                               uint32_t a2_tmem, uint32_t b2, bool first) {
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
+  for (int kk = kFrom; kk < kTo; ++kk) {
     const uint32_t acc = (first && kk == 0) ? 0u : 1u;
     mma_ts(d1, a1_tmem + static_cast<uint32_t>(kk) * 8u, desc_v(b1, kk), kIdescPV, acc);
     mma_ts(d2, a2_tmem + static_cast<uint32_t>(kk) * 8u, desc_v(b2, kk), kIdescPV, acc);
@@ -366,8 +367,9 @@ struct BwdKVCfg {
   static constexpr int kBarQDEmpty = kBarQDFull + kStages;            // 2: dV, dK of step s done
   static constexpr int kBarVecFull = kBarQDEmpty + kStages;           // 2: lse2, delta of step s (32 arrivals)
   static constexpr int kBarSTFull = kBarVecFull + kStages;            // S^T, dP^T of step s in TMEM
-  static constexpr int kBarPDSFull = kBarSTFull + 1;                  // P^T, dS^T stored (256 arrivals)
-  static constexpr int kBarDone = kBarPDSFull + 1;                    // every dV, dK product finished
+  static constexpr int kBarPDSFull = kBarSTFull + 1;                  // 2: P^T, dS^T of query half 0 / 1
+                                                                      //    stored (256 arrivals each)
+  static constexpr int kBarDone = kBarPDSFull + 2;                    // every dV, dK product finished
   static constexpr int kBarDrain = kBarDone + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
@@ -401,7 +403,7 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::kNumBars; ++i) {
       uint32_t count = 1u;
-      if (i == Cfg::kBarPDSFull) count = 256u;
+      if (i == Cfg::kBarPDSFull || i == Cfg::kBarPDSFull + 1) count = 256u;
       if (i >= Cfg::kBarVecFull && i < Cfg::kBarVecFull + Cfg::kStages) count = 32u;
       mbar_init(bar(i), count);
     }
@@ -472,9 +474,12 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     }
   } else if (warp == Cfg::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    // per step: S^T = K Q^T, dP^T = V dO^T | (P^T, dS^T stored) dV += P^T dO,
-    // dK += dS^T Q.  P^T and dS^T overwrite S^T and dP^T, whose next values
-    // are issued after these products (in issue order).
+    // per step: S^T = K Q^T, dP^T = V dO^T | (P^T, dS^T of queries 0-63
+    // stored) K steps 0-3 of dV += P^T dO, dK += dS^T Q | (queries 64-127)
+    // K steps 4-7.  The first four steps read only the columns the first
+    // half wrote, so they run while the second half is computed.  P^T and
+    // dS^T overwrite S^T and dP^T, whose next values are issued after these
+    // products (in issue order).
     if (lane == 0 && !skip) {
       bool ok = mbar_wait(bar(Cfg::kBarKV), 0, abort_flag, args.err, kDevTimeoutTma);
       for (int s = 0; s < n_steps && ok; ++s) {
@@ -490,8 +495,13 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         ok = mbar_wait(bar(Cfg::kBarPDSFull), s & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
-        issue_pv_pair(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, tmem_base + Cfg::kColDK,
-                      tmem_base + Cfg::kColDPT, q_s, s == 0);
+        issue_pv_pair<0, 4>(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, tmem_base + Cfg::kColDK,
+                            tmem_base + Cfg::kColDPT, q_s, s == 0);
+        ok = mbar_wait(bar(Cfg::kBarPDSFull + 1), s & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv_pair<4, 8>(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, tmem_base + Cfg::kColDK,
+                            tmem_base + Cfg::kColDPT, q_s, false);
         tc_commit(bar(Cfg::kBarQDEmpty + slot));
       }
       if (ok) tc_commit(bar(Cfg::kBarDone));
@@ -549,10 +559,10 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         // same buffers; those fp32 columns were read in half 0
         tmem_st_16x128b_x8(tmem_base + Cfg::kColST + lane_off + 32u * half, pp);
         tmem_st_16x128b_x8(tmem_base + Cfg::kColDPT + lane_off + 32u * half, dd);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(Cfg::kBarPDSFull + half));
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(Cfg::kBarPDSFull));
     }
     if (ok) ok = mbar_wait(bar(Cfg::kBarDone), 0, abort_flag, args.err, kDevTimeoutMma);
     ok = __all_sync(0xffffffffu, ok);
