@@ -18,8 +18,12 @@
 //     the functions below; data-dependent choices (when the reference max
 //     moves, which keys are masked) are per row only.
 //  C4 One normalisation: o = bf16_rn(O * rcp_rn(l)).
-//  C5 No split of the KV range (a split would be a fixed, length-determined
-//     partition folded identically by every entry point).
+//  C5 No split of the KV range in the default mode.  The segmented mode
+//     (opt-in, the same seg_tiles for every entry point of the mode) cuts a
+//     row's key tiles into segments of seg_tiles tiles anchored at tile 0;
+//     each segment runs C1-C3 from the fresh state (its first P V clears the
+//     accumulator) and the segments are folded left to right by fold_state /
+//     fold_o below, then C4.  One segment folds to the default mode's bits.
 //
 // Every floating-point operation below is an explicit round-to-nearest
 // intrinsic, so the compiler cannot contract or reorder them differently in
@@ -247,5 +251,31 @@ __device__ __forceinline__ void normalise32(const uint32_t (&o)[32], float inv_l
 }
 
 __device__ __forceinline__ float row_inv_l(const RowState& st) { return __frcp_rn(st.l); }
+
+// C5 fold of a segment's (m, mc, l, O) into the accumulated (m, mc, l, O) of
+// the segments before it: both are brought to the larger reference max M,
+// the side already at M by exactly 1, the other by 2^(m c - M c):
+//   l <- fma(l_acc, a, l_seg * b),   O <- fma(O_acc, a, O_seg * b).
+// The first segment is taken as it is (no fold).
+struct FoldScale {
+  float a;  // factor of the accumulated segments
+  float b;  // factor of the new segment
+};
+
+__device__ __forceinline__ FoldScale fold_state(RowState& acc, const RowState& seg) {
+  const float c = score_scale_log2();
+  const bool keep = acc.m >= seg.m;
+  const float mc = keep ? acc.mc : seg.mc;                 // M * c, as computed when M was set
+  const float a = keep ? 1.0f : ex2_approx(__fmaf_rn(acc.m, c, -mc));
+  const float b = (seg.m >= acc.m) ? 1.0f : ex2_approx(__fmaf_rn(seg.m, c, -mc));
+  acc.l = __fmaf_rn(acc.l, a, __fmul_rn(seg.l, b));
+  acc.m = keep ? acc.m : seg.m;
+  acc.mc = mc;
+  return FoldScale{a, b};
+}
+
+__device__ __forceinline__ float fold_o(float o_acc, float o_seg, FoldScale f) {
+  return __fmaf_rn(o_acc, f.a, __fmul_rn(o_seg, f.b));
+}
 
 }  // namespace kb

@@ -94,9 +94,11 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = args.B * args.Hkv;
-  const int sub = blockIdx.x / bh;
-  const int b = (blockIdx.x % bh) / args.Hkv;
-  const int g = blockIdx.x % args.Hkv;
+  const int seg = (args.seg_tiles > 0) ? static_cast<int>(blockIdx.x) / (args.n_sub * bh) : 0;
+  const int cta = (args.seg_tiles > 0) ? static_cast<int>(blockIdx.x) % (args.n_sub * bh) : static_cast<int>(blockIdx.x);
+  const int sub = cta / bh;
+  const int b = (cta % bh) / args.Hkv;
+  const int g = cta % args.Hkv;
 
   // Absolute position of query row 0, the sub-chunk's rows [r0, r1) and the
   // key range of the sequence (keys at or beyond seq_kv are never used).
@@ -127,6 +129,15 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   if (Lc <= 0) return;                                  // the chunk does not reach a second tile
   const int n_rows = kGroup * Lc;                       // packed rows in use
   const int n_kv = (pos0 + r1 - 1) / kTileKeys + 1;     // C1: KV tiles 0..floor(last position / 128)
+  // the tiles this CTA runs: all of them, or one C5 segment
+  int j0 = 0, j1 = n_kv;
+  if (args.seg_tiles > 0) {
+    j0 = seg * args.seg_tiles;
+    if (j0 >= n_kv) return;                             // the rows end before this segment
+    j1 = min(n_kv, j0 + args.seg_tiles);
+  }
+  const int nt = j1 - j0;
+  const bool has_last = (j1 == n_kv);
   const bool zero_tail = (args.block_table != nullptr) || (args.ctx_lens != nullptr) || (args.starts != nullptr);
   const int tail_from = seq_kv - (n_kv - 1) * kTileKeys;   // first V row of the last tile past the sequence
 
@@ -176,12 +187,12 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       const uint64_t stream_once = l2_policy_evict_first();
       int issued = 0;
       bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int slot = j % Cfg::kStages;
-        const uint32_t use = j / Cfg::kStages;
+      for (int jj = 0; jj < nt && ok; ++jj) {
+        const int slot = jj % Cfg::kStages;
+        const uint32_t use = jj / Cfg::kStages;
         int row = 0, plane = 0;
-        if (lane == 0) kv_tile_coords(args, b, g, j, row, plane);
-        if (j >= Cfg::kStages)
+        if (lane == 0) kv_tile_coords(args, b, g, j0 + jj, row, plane);
+        if (jj >= Cfg::kStages)
           ok = mbar_wait(bar(Cfg::kBarKEmpty + slot), (use - 1) & 1, abort_flag, args.err, kDevTimeoutSlot);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -190,8 +201,8 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           mbar_arrive_expect_tx(bar(Cfg::kBarKFull + slot), kTileBytes);
           tma_load_tile_hint(kdst, &tmap_k, row, plane, bar(Cfg::kBarKFull + slot), stream_once);
         }
-        issued = 2 * j + 1;
-        if (j >= Cfg::kStages)
+        issued = 2 * jj + 1;
+        if (jj >= Cfg::kStages)
           ok = mbar_wait(bar(Cfg::kBarVEmpty + slot), (use - 1) & 1, abort_flag, args.err, kDevTimeoutSlot);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -200,12 +211,12 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           mbar_arrive_expect_tx(bar(Cfg::kBarVFull + slot), kTileBytes);
           tma_load_tile_hint(vdst, &tmap_v, row, plane, bar(Cfg::kBarVFull + slot), stream_once);
         }
-        issued = 2 * j + 2;
+        issued = 2 * jj + 2;
       }
-      if (ok && zero_tail) {
+      if (ok && zero_tail && has_last) {
         // V rows past the sequence in its last tile may hold anything (another
         // sequence's data, NaN): make them zero so P = 0 contributes nothing.
-        const int jl = n_kv - 1;
+        const int jl = nt - 1;
         const int slot = jl % Cfg::kStages;
         ok = mbar_wait(bar(Cfg::kBarVFull + slot), (jl / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
         ok = __all_sync(0xffffffffu, ok);
@@ -241,8 +252,8 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         tc_commit(bar(Cfg::kBarSFull));
         tc_commit(bar(Cfg::kBarKEmpty));
       }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        if (j + 1 < n_kv) {
+      for (int j = 0; j < nt && ok; ++j) {                  // j: tile j0 + j, ring and buffer index
+        if (j + 1 < nt) {
           const int jn = j + 1;
           const int slot = jn % Cfg::kStages;
           ok = mbar_wait(bar(Cfg::kBarKFull + slot), (jn / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
@@ -261,7 +272,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         ok = mbar_wait(bar(Cfg::kBarPFull + j % Cfg::kSBufs), (j / Cfg::kSBufs) & 1, abort_flag, args.err,
                        kDevTimeoutSoftmax);
         if (ok) {
-          if (zero_tail && j == n_kv - 1)
+          if (zero_tail && has_last && j == nt - 1)
             ok = mbar_wait(bar(Cfg::kBarVReady), 0, abort_flag, args.err, kDevTimeoutTma);
           else
             ok = mbar_wait(bar(Cfg::kBarVFull + slot), (j / Cfg::kStages) & 1, abort_flag, args.err,
@@ -270,7 +281,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if (!ok) break;
         tc_fence_after();
         issue_pv(tmem_base + Cfg::kOCol, tmem_base + (j % Cfg::kSBufs) * 128u, sbase + Cfg::kVOff + slot * kTileBytes,
-                 j == 0);
+                 j == 0);                                   // the range's first tile clears O
         tc_commit(bar(Cfg::kBarOFull + j % Cfg::kSBufs));
         tc_commit(bar(Cfg::kBarVEmpty + slot));
       }
@@ -289,7 +300,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     const int pos = pos0 + r;
     RowState st = row_state_init();
     bool ok = !skip;
-    for (int j = 0; j < n_kv && ok; ++j) {
+    for (int j = 0; j < nt && ok; ++j) {                    // j: tile j0 + j
       ok = mbar_wait(bar(Cfg::kBarSFull + j % Cfg::kSBufs), (j / Cfg::kSBufs) & 1, abort_flag, args.err,
                      kDevTimeoutMma);
       ok = __all_sync(0xffffffffu, ok);
@@ -299,8 +310,9 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       uint32_t s[128];
       tmem_ld128_wait(s_tmem, s);
       uint32_t p[64];
-      const float alpha = (j == n_kv - 1) ? row_softmax_tile<true>(s, pos - j * kTileKeys + 1, st, p)
-                                          : row_softmax_tile<false>(s, kTileKeys, st, p);
+      const int jt = j0 + j;
+      const float alpha = (jt == n_kv - 1) ? row_softmax_tile<true>(s, pos - jt * kTileKeys + 1, st, p)
+                                           : row_softmax_tile<false>(s, kTileKeys, st, p);
       // O is rescaled only when some row's reference max moved, and only then
       // must the previous tile's P V have finished (its barrier is that tile's
       // S buffer's; the MMA issuer's wait before reusing an S buffer keeps it
@@ -332,10 +344,29 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       mbar_arrive(bar(Cfg::kBarPFull + j % Cfg::kSBufs));
     }
     if (ok)
-      ok = mbar_wait(bar(Cfg::kBarOFull + (n_kv - 1) % Cfg::kSBufs), ((n_kv - 1) / Cfg::kSBufs) & 1, abort_flag,
+      ok = mbar_wait(bar(Cfg::kBarOFull + (nt - 1) % Cfg::kSBufs), ((nt - 1) / Cfg::kSBufs) & 1, abort_flag,
                      args.err, kDevTimeoutMma);
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+    if (ok && args.part != nullptr) {
+      // C5: this segment's partial (O unnormalised, m, mc, l) for the fold
+      tc_fence_after();
+      const bool store = m < n_rows;
+      float* dst = args.part + ((((static_cast<size_t>(b) * args.Hq + g * kGroup + head) * args.L + r) * args.n_seg +
+                                 seg) * kPartFloats);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32_wait(o_tmem + c * 32u, o);                // collective: every lane loads
+        if (store) {
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            reinterpret_cast<float4*>(dst + 32 * c)[v4] =
+                make_float4(__uint_as_float(o[4 * v4]), __uint_as_float(o[4 * v4 + 1]),
+                            __uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3]));
+        }
+      }
+      if (store) reinterpret_cast<float4*>(dst + 128)[0] = make_float4(st.m, st.mc, st.l, 0.0f);
+    } else if (ok) {
       tc_fence_after();
       const float inv_l = row_inv_l(st);
       const bool store = m < n_rows;
@@ -367,7 +398,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     const int pos = pos0 + r;
     RowState st = row_state_init();
     bool ok = !skip;
-    for (int j = 0; j < n_kv && ok; ++j) {
+    for (int j = 0; j < nt && ok; ++j) {                    // j: tile j0 + j
       ok = mbar_wait(bar(Cfg::kBarSFull + j % Cfg::kSBufs), (j / Cfg::kSBufs) & 1, abort_flag, args.err,
                      kDevTimeoutMma);
       ok = __all_sync(0xffffffffu, ok);
@@ -388,8 +419,9 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
       }
       uint32_t p[16];
-      const float alpha = (j == n_kv - 1) ? row_softmax_tile_quad<true>(x, u, pos - j * kTileKeys + 1, st, p)
-                                          : row_softmax_tile_quad<false>(x, u, kTileKeys, st, p);
+      const int jt = j0 + j;
+      const float alpha = (jt == n_kv - 1) ? row_softmax_tile_quad<true>(x, u, pos - jt * kTileKeys + 1, st, p)
+                                           : row_softmax_tile_quad<false>(x, u, kTileKeys, st, p);
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
         // rescale O (rows in lanes 0..31 through the 32x32b shape; lane L takes
         // the factor of row L % 8, rows 8..31 are never stored)
@@ -418,10 +450,35 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       mbar_arrive(bar(Cfg::kBarPFull + j % Cfg::kSBufs));
     }
     if (ok)
-      ok = mbar_wait(bar(Cfg::kBarOFull + (n_kv - 1) % Cfg::kSBufs), ((n_kv - 1) / Cfg::kSBufs) & 1, abort_flag,
+      ok = mbar_wait(bar(Cfg::kBarOFull + (nt - 1) % Cfg::kSBufs), ((nt - 1) / Cfg::kSBufs) & 1, abort_flag,
                      args.err, kDevTimeoutMma);
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+    if (ok && args.part != nullptr) {
+      // C5: lane L < 8 writes row L's partial; the state comes from its quad
+      tc_fence_after();
+      const float m_lane = __shfl_sync(0xffffffffu, st.m, 4 * (lane & 7));
+      const float mc_lane = __shfl_sync(0xffffffffu, st.mc, 4 * (lane & 7));
+      const float l_lane = __shfl_sync(0xffffffffu, st.l, 4 * (lane & 7));
+      const int row = lane;
+      const bool store = row < n_rows;
+      const int s_head = store ? row / Lc : 0;
+      const int s_r = store ? r0 + row % Lc : r0;
+      float* dst = args.part + ((((static_cast<size_t>(b) * args.Hq + g * kGroup + s_head) * args.L + s_r) *
+                                 args.n_seg + seg) * kPartFloats);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32_wait(o_tmem + c * 32u, o);
+        if (store) {
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            reinterpret_cast<float4*>(dst + 32 * c)[v4] =
+                make_float4(__uint_as_float(o[4 * v4]), __uint_as_float(o[4 * v4 + 1]),
+                            __uint_as_float(o[4 * v4 + 2]), __uint_as_float(o[4 * v4 + 3]));
+        }
+      }
+      if (store) reinterpret_cast<float4*>(dst + 128)[0] = make_float4(m_lane, mc_lane, l_lane, 0.0f);
+    } else if (ok) {
       tc_fence_after();
       // lane L < 8 stores row L; its l comes from the quad that owns the row
       const float l_lane = __shfl_sync(0xffffffffu, st.l, 4 * (lane & 7));
@@ -471,7 +528,7 @@ static cudaError_t launch_packed_t(const CUtensorMap& tk, const CUtensorMap& tv,
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const unsigned grid = static_cast<unsigned>(n_sub * a.B * a.Hkv);
+  const unsigned grid = static_cast<unsigned>((a.seg_tiles > 0 ? a.n_seg : 1) * n_sub * a.B * a.Hkv);
   kb_decode_kernel<kWide><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(tk, tv, a);
   return cudaGetLastError();
 }

@@ -135,7 +135,8 @@ struct Ragged {
 
 kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int L, int start,
                      int kv_cap, int q_tiles_per_cta, void* stream, const Paging* paging = nullptr,
-                     const Ragged* ragged = nullptr, float* lse = nullptr) {
+                     const Ragged* ragged = nullptr, float* lse = nullptr, int seg_tiles = 0,
+                     void* workspace = nullptr, size_t workspace_bytes = 0) {
   kb_status s = check_ptrs(q, k, v, o);
   if (s != KB_OK) return s;
   if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
@@ -145,6 +146,23 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   if (q_tiles_per_cta < 0 || q_tiles_per_cta > kb::kShapeOneTilePerSm) return KB_ERR_INVALID_ARG;
   if (q_tiles_per_cta == 0 && L > kb::kMaxPackedRows) return KB_ERR_INVALID_ARG;
   if (lse != nullptr && q_tiles_per_cta != kb::kShapeOneTilePerSm) return KB_ERR_INVALID_ARG;
+  if (seg_tiles < 0) return KB_ERR_INVALID_ARG;
+  if (seg_tiles > 0) {
+    // the segmented mode runs on the packed kernel (with a workspace) and the
+    // one-tile-per-SM kernel, contiguous caches, no log-sum-exp
+    if (paging || ragged || lse) return KB_ERR_UNSUPPORTED;
+    if (q_tiles_per_cta != 0 && q_tiles_per_cta != kb::kShapeOneTilePerSm) return KB_ERR_INVALID_ARG;
+    if (q_tiles_per_cta == 0) {
+      // the packed kernel leaves per-segment partials in the caller's workspace
+      const int n_kv = (start + L - 1) / kb::kTileKeys + 1;
+      const long long n_seg = (n_kv + seg_tiles - 1) / seg_tiles;
+      const unsigned long long need =
+          static_cast<unsigned long long>(B) * Hq * L * n_seg * kb::kPartFloats * sizeof(float);
+      if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return KB_ERR_INVALID_ARG;
+      if (n_seg * 2LL * B * Hkv > 0x7FFFFFFFLL) return KB_ERR_UNSUPPORTED;
+    }
+  }
   // a ragged batch sizes the grid for its longest possible sequence
   const int first_tile = ragged ? 0 : start / kb::kTileRows;
   const int last_tile = ragged ? (L + kb::kTileRows - 2) / kb::kTileRows : (start + L - 1) / kb::kTileRows;
@@ -183,6 +201,14 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   if ((s = encode_rows_map(&tv, v, kv_rows, kv_planes, kv_stride)) != KB_OK) return s;
   if (q_tiles_per_cta == 0) {
     // query rows packed by GQA group
+    const int split = std::min(L, kb::kTileKeys - start % kb::kTileKeys);
+    const int n_sub = (ragged || split < L) ? 2 : 1;
+    int n_seg = 0;
+    if (seg_tiles > 0) {
+      const int n_kv = (start + L - 1) / kb::kTileKeys + 1;
+      n_seg = (n_kv + seg_tiles - 1) / seg_tiles;
+      if ((s = check_device_pointer(workspace)) != KB_OK) return s;
+    }
     kb::PackedArgs a{};
     a.q = q;
     a.o = o;
@@ -203,9 +229,16 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
       a.num_pages = paging->num_pages;
     }
     a.err = dst->err;
-    const int split = std::min(L, kb::kTileKeys - start % kb::kTileKeys);
-    const int n_sub = (ragged || split < L) ? 2 : 1;
-    const cudaError_t e = kb::launch_packed(tk, tv, a, n_sub, static_cast<cudaStream_t>(stream));
+    a.n_sub = n_sub;
+    if (seg_tiles > 0) {
+      a.seg_tiles = seg_tiles;
+      a.n_seg = n_seg;
+      a.part = static_cast<float*>(workspace);
+    }
+    cudaError_t e = kb::launch_packed(tk, tv, a, n_sub, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess && seg_tiles > 0)
+      e = kb::launch_seg_fold(static_cast<const float*>(workspace), o, static_cast<long long>(B) * Hq * L, L, start,
+                              seg_tiles, n_seg, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return KB_OK;
   }
@@ -227,6 +260,7 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   // share K/V in L2; below that, globally longest tile first
   a.group_major = grid > 4LL * dst->sm_count ? 1 : 0;
   a.lse = lse;
+  a.seg_tiles = seg_tiles;
   if (ragged) {
     a.starts = ragged->starts;
     a.lens = ragged->lens;
@@ -268,6 +302,36 @@ kb_status kb_attn_prefill(const void* q, const void* k, const void* v, void* o, 
                           void* stream) {
   if (S < 1) return KB_ERR_INVALID_ARG;
   return chunk_impl(q, k, v, o, B, Hq, Hkv, S, 0, S, chunk_cta_shape(S), stream);
+}
+
+kb_status kb_attn_prefill_seg(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int S,
+                              int seg_tiles, void* stream) {
+  if (S < 1 || seg_tiles < 1) return KB_ERR_INVALID_ARG;
+  return chunk_impl(q, k, v, o, B, Hq, Hkv, S, 0, S, kb::kShapeOneTilePerSm, stream, nullptr, nullptr, nullptr,
+                    seg_tiles);
+}
+
+size_t kb_attn_seg_workspace_bytes(int B, int Hq, int L, int start, int seg_tiles) {
+  if (B < 1 || Hq < 1 || L < 1 || start < 0 || seg_tiles < 1 || L > kb::kMaxPackedRows) return 0;
+  const int n_kv = (start + L - 1) / kb::kTileKeys + 1;
+  const int n_seg = (n_kv + seg_tiles - 1) / seg_tiles;
+  return static_cast<size_t>(B) * Hq * L * n_seg * kb::kPartFloats * sizeof(float);
+}
+
+kb_status kb_attn_chunk_seg(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int L,
+                            int start, int kv_cap, int seg_tiles, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (seg_tiles < 1) return KB_ERR_INVALID_ARG;
+  return chunk_impl(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, chunk_cta_shape(L), stream, nullptr, nullptr, nullptr,
+                    seg_tiles, workspace, workspace_bytes);
+}
+
+kb_status kb_attn_decode_seg(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                             int ctx_len, int kv_cap, int seg_tiles, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (ctx_len < 1 || ctx_len > kv_cap || seg_tiles < 1) return KB_ERR_INVALID_ARG;
+  return chunk_impl(q, k, v, o, B, Hq, Hkv, 1, ctx_len - 1, kv_cap, 0, stream, nullptr, nullptr, nullptr, seg_tiles,
+                    workspace, workspace_bytes);
 }
 
 kb_status kb_attn_prefill_lse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,

@@ -22,6 +22,7 @@ struct PrefillArgs {
   int kv_cap;              // keys per sequence the cache can hold
   int group_major;         // CTA order: 1 = (b, g) slowest, 0 = query tile slowest
   float* lse;              // optional [B, Hq, L] fp32: natural-log log-sum-exp of each row's scaled scores
+  int seg_tiles;           // C5 segmented mode: segment length in key tiles (0 = default mode)
   uint32_t* err;    // device error word
 };
 
@@ -38,8 +39,16 @@ struct PackedArgs {
   int pages_per_seq, page_size, num_pages;
   const int* starts;       // optional device [B]: per-sequence start and row count (ragged
   const int* lens;         //   batch); L is then the row stride of q and o
+  int n_sub;               // sub-chunks per (b, kv head) in the grid (1 or 2)
+  // segmented mode (seg_tiles > 0): CTA (seg, sub, b, g) runs key tiles
+  // [seg * seg_tiles, +seg_tiles) from the fresh state and writes the rows'
+  // partial (O[128], m, mc, l) to part[((b*Hq + h)*L + r)*n_seg + seg][132]
+  int seg_tiles, n_seg;
+  float* part;
   uint32_t* err;
 };
+
+constexpr int kPartFloats = 132;   // one partial: O[128], m, mc, l, pad
 
 constexpr int kMaxPackedRows = 32;   // query rows per (batch, head) the packed kernel takes
 
@@ -74,6 +83,10 @@ struct BwdArgs {
 // tq, tdo: [B*Hq planes, S rows]; tk, tv: [B*Hkv planes, S rows].
 cudaError_t launch_backward(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t s);
+// C5 fold of the packed kernel's per-segment partials, one warp per row
+// (rows = B*Hq*L, row r of a (b, h) at position start + r), then C4 into o.
+cudaError_t launch_seg_fold(const float* part, void* o, long long rows, int L, int start, int seg_tiles, int n_seg,
+                            cudaStream_t s);
 cudaError_t launch_wait_probe(uint32_t* err, unsigned long long limit_ns, cudaStream_t s);
 
 }  // namespace kb

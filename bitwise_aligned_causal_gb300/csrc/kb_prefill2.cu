@@ -22,16 +22,20 @@
 
 namespace kb {
 
+// kSeg: the C5 segmented mode -- two S buffers, the segment's O and the
+// folded O in TMEM (2*128 + 128 + 128 columns), two-stage K/V rings.
+template <bool kSeg>
 struct Prefill2Cfg {
   static constexpr int kThreads = 384;
   static constexpr int kLoadWarpK = 8;
   static constexpr int kMmaWarp = 9;                        // TMEM allocator + Q K^T issuer
   static constexpr int kLoadWarpV = 10;
   static constexpr int kPvWarp = 11;                        // P V issuer
-  static constexpr int kStages = 3;
-  static constexpr int kSBufs = 3;                          // = kStages: K slot j%3 frees when S(j) lands
-  static constexpr uint32_t kTmemCols = 512;                // S0, S1, S2, O (128 columns each)
-  static constexpr uint32_t kOCol = kSBufs * 128u;
+  static constexpr int kStages = kSeg ? 2 : 3;
+  static constexpr int kSBufs = kStages;                    // K slot j%n frees when S(j) lands
+  static constexpr uint32_t kTmemCols = 512;                // S0, S1, S2, O (or S0, S1, O_seg, O_acc)
+  static constexpr uint32_t kOCol = kSBufs * 128u;          // O of the running segment
+  static constexpr uint32_t kOAccCol = 384u;                // folded O (segmented mode)
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = kTileBytes;
   static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
@@ -39,8 +43,8 @@ struct Prefill2Cfg {
   static constexpr int kBarQFull = 0;
   static constexpr int kBarKFull = 1;
   static constexpr int kBarVFull = kBarKFull + kStages;
-  // per S buffer j%3: S(j) written (also: K slot j%3 free), P(j) written
-  // (256 arrivals), P V(j) finished (also: V slot j%3 free)
+  // per S buffer j%n: S(j) written (also: K slot j%n free), P(j) written
+  // (256 arrivals), P V(j) finished (also: V slot j%n free)
   static constexpr int kBarSFull = kBarVFull + kStages;
   static constexpr int kBarPFull = kBarSFull + kSBufs;
   static constexpr int kBarOFull = kBarPFull + kSBufs;
@@ -58,10 +62,11 @@ __device__ __forceinline__ void drain_wait2(uint32_t bar, uint32_t parity) {
     if (global_timer_ns() - t0 > 50000000ull) break;
 }
 
-__global__ void __launch_bounds__(Prefill2Cfg::kThreads, 1)
+template <bool kSeg>
+__global__ void __launch_bounds__(Prefill2Cfg<kSeg>::kThreads, 1)
 kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs args) {
-  using Cfg = Prefill2Cfg;
+  using Cfg = Prefill2Cfg<kSeg>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_addr(smem);
@@ -240,7 +245,9 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         }
         if (!ok) break;
         tc_fence_after();
-        issue_pv(tmem_base + Cfg::kOCol, tmem_base + sb * 128u, sbase + Cfg::kVOff + sb * kTileBytes, j == 0);
+        // the first tile (of each segment, in segmented mode) clears O
+        const bool first = kSeg ? (j % args.seg_tiles == 0) : (j == 0);
+        issue_pv(tmem_base + Cfg::kOCol, tmem_base + sb * 128u, sbase + Cfg::kVOff + sb * kTileBytes, first);
         tc_commit(bar(Cfg::kBarOFull + sb));
       }
       if (!ok) {
@@ -257,8 +264,11 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     const int rA = lane_base + (lane >> 2);                         // rows (TMEM lanes) of this thread
     const int rB = rA + 8;
     const uint32_t o_tmem = tmem_base + Cfg::kOCol + lane_off;
+    const uint32_t oacc_tmem = tmem_base + Cfg::kOAccCol + lane_off;   // segmented mode only
     RowState sA = row_state_init();
     RowState sB = row_state_init();
+    RowState accA = row_state_init();                               // folded segments (segmented mode)
+    RowState accB = row_state_init();
     bool ok = !skip;
     for (int j = 0; j < n_kv && ok; ++j) {
       const int sb = j % Cfg::kSBufs;
@@ -287,6 +297,11 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           xB[16 + 2 * r + 1] = __uint_as_float(v[4 * r + 3]);
         }
       }
+      const bool seg_start = kSeg && (j % args.seg_tiles == 0);
+      if (seg_start) {                                              // C5: each segment starts fresh
+        sA = row_state_init();
+        sB = row_state_init();
+      }
       uint32_t pA[16], pB[16];
       float aA, aB;
       if (j == n_kv - 1) {                                          // diagonal tile: causal mask
@@ -296,7 +311,7 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         aA = row_softmax_tile_quad<false>(xA, u, kTileKeys, sA, pA);
         aB = row_softmax_tile_quad<false>(xB, u, kTileKeys, sB, pB);
       }
-      if (j > 0 && __any_sync(0xffffffffu, aA != 1.0f || aB != 1.0f)) {
+      if (j > 0 && !seg_start && __any_sync(0xffffffffu, aA != 1.0f || aB != 1.0f)) {
         // O must hold P V of tile j-1 before it is rescaled; per-buffer
         // barriers keep this wait exact although it is only taken when needed
         // (P V(j-4) is done: S(j) was committed after it)
@@ -332,6 +347,48 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(Cfg::kBarPFull + sb));
+      if constexpr (kSeg) {
+        if (j % args.seg_tiles == args.seg_tiles - 1 || j == n_kv - 1) {
+          // C5: the segment ends here; fold its (m, mc, l, O) into the
+          // accumulated segments once its last P V has finished
+          ok = mbar_wait(bar(Cfg::kBarOFull + sb), (j / Cfg::kSBufs) & 1, abort_flag, args.err, kDevTimeoutMma);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+          const bool first_seg = j < args.seg_tiles;
+          FoldScale fA{1.0f, 1.0f}, fB{1.0f, 1.0f};
+          if (first_seg) {
+            accA = sA;
+            accB = sB;
+          } else {
+            fA = fold_state(accA, sA);
+            fB = fold_state(accB, sB);
+          }
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t os[32], oa[32];
+            tmem_ld_16x256b_x8_wait(o_tmem + 64u * half, os);
+            if (first_seg) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) oa[i] = os[i];
+            } else {
+              tmem_ld_16x256b_x8_wait(oacc_tmem + 64u * half, oa);
+#pragma unroll
+              for (int r = 0; r < 8; ++r) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  oa[4 * r + e] = __float_as_uint(fold_o(__uint_as_float(oa[4 * r + e]),
+                                                         __uint_as_float(os[4 * r + e]), fA));
+                  oa[4 * r + 2 + e] = __float_as_uint(fold_o(__uint_as_float(oa[4 * r + 2 + e]),
+                                                             __uint_as_float(os[4 * r + 2 + e]), fB));
+                }
+              }
+            }
+            tmem_st_16x256b_x8(oacc_tmem + 64u * half, oa);
+          }
+          tmem_st_wait();
+        }
+      }
     }
     if (ok)
       ok = mbar_wait(bar(Cfg::kBarOFull + (n_kv - 1) % Cfg::kSBufs), ((n_kv - 1) / Cfg::kSBufs) & 1, abort_flag,
@@ -339,13 +396,14 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     ok = __all_sync(0xffffffffu, ok);
     if (ok) {
       tc_fence_after();
-      const float invA = row_inv_l(sA);
-      const float invB = row_inv_l(sB);
+      const float invA = row_inv_l(kSeg ? accA : sA);
+      const float invB = row_inv_l(kSeg ? accB : sB);
+      const uint32_t o_out = kSeg ? oacc_tmem : o_tmem;
       const int iA = t * kTileRows + rA - start;                     // query row index in q / o
       const int iB = iA + 8;
       const bool stA = (iA >= 0) && (iA < L);
       const bool stB = (iB >= 0) && (iB < L);
-      if (args.lse != nullptr && u == 0) {
+      if (!kSeg && args.lse != nullptr && u == 0) {
         // natural-log log-sum-exp of the row's scaled scores: the weights are
         // 2^(s c - mc), so log2 sum_j 2^(s_j c) = mc + log2(l)
         constexpr float kLn2 = 0.69314718055994531f;
@@ -360,7 +418,7 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint32_t o[32];
-        tmem_ld_16x256b_x8_wait(o_tmem + 64u * half, o);
+        tmem_ld_16x256b_x8_wait(o_out + 64u * half, o);
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           const int col = 64 * half + 8 * r + 2 * u;                 // this thread's two columns
@@ -384,23 +442,29 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
   }
 }
 
-cudaError_t launch_prefill_s2(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const PrefillArgs& a, cudaStream_t s) {
-  using Cfg = Prefill2Cfg;
+template <bool kSeg>
+static cudaError_t launch_prefill_s2_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                       const PrefillArgs& a, cudaStream_t s) {
+  using Cfg = Prefill2Cfg<kSeg>;
   static_assert(Cfg::kSmemBytes <= 227u * 1024u, "shared memory budget");
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(kb_prefill_kernel_s2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(kb_prefill_kernel_s2<kSeg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Cfg::kSmemBytes));
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   const long long grid = static_cast<long long>(a.n_tiles) * a.B * a.Hq;
-  kb_prefill_kernel_s2<<<static_cast<unsigned>(grid), Cfg::kThreads, Cfg::kSmemBytes, s>>>(tq, tk, tv, a);
+  kb_prefill_kernel_s2<kSeg><<<static_cast<unsigned>(grid), Cfg::kThreads, Cfg::kSmemBytes, s>>>(tq, tk, tv, a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_s2(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const PrefillArgs& a, cudaStream_t s) {
+  return a.seg_tiles > 0 ? launch_prefill_s2_t<true>(tq, tk, tv, a, s) : launch_prefill_s2_t<false>(tq, tk, tv, a, s);
 }
 
 }  // namespace kb

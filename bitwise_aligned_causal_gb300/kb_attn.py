@@ -40,6 +40,10 @@ _SIGS = {
     "kb_attn_debug_wait_timeout": [_I, _P],
     "kb_attn_chunk_cta_shape": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P],
     "kb_attn_prefill_lse": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P],
+    "kb_attn_prefill_seg": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P],
+    "kb_attn_chunk_seg": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P],
+    "kb_attn_decode_seg": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P],
+    "kb_attn_seg_workspace_bytes": [_I, _I, _I, _I, _I],
     "kb_attn_backward": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P],
     "kb_status_string": [_I],
     "kb_contract_version": [],
@@ -49,7 +53,8 @@ _SIGS = {
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
-    _f.restype = ctypes.c_char_p if _name.endswith("string") else ctypes.c_int
+    _f.restype = (ctypes.c_char_p if _name.endswith("string")
+                  else ctypes.c_size_t if _name.endswith("_bytes") else ctypes.c_int)
 
 EXPORTED = tuple(_SIGS)
 
@@ -121,6 +126,26 @@ def kb_attn_prefill_lse(q, k, v, o, lse, B, Hq, Hkv, S, stream=None) -> int:
 
 def kb_attn_backward(q, k, v, o, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, stream=None) -> int:
     return _lib.kb_attn_backward(q, k, v, o, dout, lse, delta, dq, dk, dv, B, Hq, Hkv, S, stream)
+
+
+def kb_attn_prefill_seg(q, k, v, o, B, Hq, Hkv, S, seg_tiles, stream=None) -> int:
+    return _lib.kb_attn_prefill_seg(q, k, v, o, B, Hq, Hkv, S, seg_tiles, stream)
+
+
+def kb_attn_chunk_seg(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, seg_tiles, workspace, workspace_bytes,
+                      stream=None) -> int:
+    return _lib.kb_attn_chunk_seg(q, k, v, o, B, Hq, Hkv, L, start, kv_cap, seg_tiles, workspace, workspace_bytes,
+                                  stream)
+
+
+def kb_attn_decode_seg(q, k, v, o, B, Hq, Hkv, ctx_len, kv_cap, seg_tiles, workspace, workspace_bytes,
+                       stream=None) -> int:
+    return _lib.kb_attn_decode_seg(q, k, v, o, B, Hq, Hkv, ctx_len, kv_cap, seg_tiles, workspace, workspace_bytes,
+                                   stream)
+
+
+def kb_attn_seg_workspace_bytes(B, Hq, L, start, seg_tiles) -> int:
+    return int(_lib.kb_attn_seg_workspace_bytes(B, Hq, L, start, seg_tiles))
 
 
 def kb_attn_check_device_status(stream=None) -> int:
@@ -318,3 +343,52 @@ def backward(q, k, v, o, dout, lse, delta=None, dq=None, dk=None, dv=None, strea
                             delta.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, S,
                             _stream(stream)), "kb_attn_backward")
     return dq, dk, dv, delta
+
+
+def _workspace(nbytes, device, workspace):
+    torch = _torch()
+    if workspace is None:
+        return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+    return workspace
+
+
+def prefill_seg(q, k, v, seg_tiles, out=None, stream=None):
+    """Segmented-mode prefill (segments of seg_tiles 128-key tiles, folded left to right)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, 4)
+    B, Hq, S, _ = q.shape
+    o = _torch().empty_like(q) if out is None else out
+    _check(o, "out", 4)
+    _raise(kb_attn_prefill_seg(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, k.shape[1], S,
+                               int(seg_tiles), _stream(stream)), "kb_attn_prefill_seg")
+    return o
+
+
+def chunk_seg(q, k, v, start, seg_tiles, out=None, workspace=None, stream=None):
+    """Segmented-mode chunk: q [B,Hq,L,128] at positions start.., caches [B,Hkv,cap,128]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, 4)
+    B, Hq, L, _ = q.shape
+    o = _torch().empty_like(q) if out is None else out
+    _check(o, "out", 4)
+    ws = _workspace(kb_attn_seg_workspace_bytes(B, Hq, L, int(start), int(seg_tiles)), q.device, workspace)
+    _raise(kb_attn_chunk_seg(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, k.shape[1], L,
+                             int(start), k.shape[2], int(seg_tiles), ws.data_ptr(), ws.numel() * ws.element_size(),
+                             _stream(stream)), "kb_attn_chunk_seg")
+    return o
+
+
+def decode_seg(q, k, v, ctx_len, seg_tiles, out=None, workspace=None, stream=None):
+    """Segmented-mode decode: q [B,Hq,1,128] at position ctx_len-1."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, 4)
+    B, Hq = q.shape[0], q.shape[1]
+    o = _torch().empty_like(q) if out is None else out
+    _check(o, "out", 4)
+    ws = _workspace(kb_attn_seg_workspace_bytes(B, Hq, 1, int(ctx_len) - 1, int(seg_tiles)), q.device, workspace)
+    _raise(kb_attn_decode_seg(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, k.shape[1],
+                              int(ctx_len), k.shape[2], int(seg_tiles), ws.data_ptr(),
+                              ws.numel() * ws.element_size(), _stream(stream)), "kb_attn_decode_seg")
+    return o

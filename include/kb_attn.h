@@ -32,6 +32,8 @@
 #ifndef KB_ATTN_H
 #define KB_ATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -156,6 +158,39 @@ kb_status kb_attn_check_device_status(void* stream);
  * KB_ERR_TIMEOUT.  Faults and hangs nothing.
  */
 kb_status kb_attn_debug_wait_timeout(int limit_us, void* stream);
+
+/*
+ * Segmented mode (contract C5; SURVEY's fixed-segment split of the KV range):
+ * a row's key tiles are cut into segments of seg_tiles 128-key tiles anchored
+ * at key 0; each segment runs the default mode's tile steps from the fresh
+ * state and the segments are folded left to right by one fold function, then
+ * normalised.  Every entry point of the mode gives the same bits for a row
+ * at position p when called with the same seg_tiles (>= 1); a row whose keys
+ * fit in one segment has the default mode's bits.  The split lets a decode
+ * of a long context run one CTA per segment (small batches), at the price of
+ * an extra fold for prefill.
+ *
+ * kb_attn_prefill_seg: as kb_attn_prefill (no workspace).
+ * kb_attn_chunk_seg:   as kb_attn_chunk.  Chunks of at most 32 rows (and
+ *   decode) run one CTA per (segment, batch, KV head) and need a device
+ *   workspace of kb_attn_seg_workspace_bytes(B, Hq, L, start, seg_tiles)
+ *   bytes (16-byte aligned, caller-owned, contents scratch); longer chunks
+ *   fold in the kernel and ignore it.  Too small a workspace returns
+ *   KB_ERR_INVALID_ARG.
+ * kb_attn_decode_seg:  as kb_attn_decode (a chunk of one row at ctx_len-1).
+ * Paged and ragged caches are not offered in this mode (KB_ERR_UNSUPPORTED).
+ */
+kb_status kb_attn_prefill_seg(const void* q, const void* k, const void* v, void* o,
+                              int B, int Hq, int Hkv, int S, int seg_tiles, void* stream);
+kb_status kb_attn_chunk_seg(const void* q, const void* k, const void* v, void* o,
+                            int B, int Hq, int Hkv, int L, int start, int kv_cap, int seg_tiles,
+                            void* workspace, size_t workspace_bytes, void* stream);
+kb_status kb_attn_decode_seg(const void* q, const void* k, const void* v, void* o,
+                             int B, int Hq, int Hkv, int ctx_len, int kv_cap, int seg_tiles,
+                             void* workspace, size_t workspace_bytes, void* stream);
+/* Workspace bytes kb_attn_chunk_seg / kb_attn_decode_seg need for a chunk of
+ * L <= 32 rows at positions start..start+L-1 (0 for bad arguments or L > 32). */
+size_t kb_attn_seg_workspace_bytes(int B, int Hq, int L, int start, int seg_tiles);
 
 /*
  * Training forward: kb_attn_prefill plus each row's log-sum-exp, which the

@@ -107,6 +107,21 @@ def test_training_entry_points_reject_bad_arguments(kb):
     assert kb.kb_attn_backward(*ok, FAKE, FAKE, *outs, 1, 32, 2, 64) == kb.KB_ERR_UNSUPPORTED
 
 
+def test_segmented_mode_rejects_bad_arguments(kb):
+    args = (FAKE, FAKE, FAKE, FAKE, 1, 32, 8)
+    assert kb.kb_attn_prefill_seg(*args, 64, 0) == kb.KB_ERR_INVALID_ARG                     # seg_tiles 0
+    assert kb.kb_attn_prefill_seg(*args, 0, 2) == kb.KB_ERR_INVALID_ARG                      # S 0
+    assert kb.kb_attn_decode_seg(*args, 100, 200, 0, FAKE, 1 << 20) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_decode_seg(*args, 300, 200, 2, FAKE, 1 << 20) == kb.KB_ERR_INVALID_ARG  # ctx > cap
+    assert kb.kb_attn_decode_seg(*args, 100, 200, 2, None, 1 << 20) == kb.KB_ERR_INVALID_ARG  # no workspace
+    need = kb.kb_attn_seg_workspace_bytes(1, 32, 1, 99, 2)
+    assert need == 32 * 1 * 1 * 132 * 4
+    assert kb.kb_attn_decode_seg(*args, 100, 200, 2, FAKE, need - 1) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_decode_seg(*args, 100, 200, 2, FAKE + 8, need) == kb.KB_ERR_INVALID_ARG  # misaligned
+    assert kb.kb_attn_seg_workspace_bytes(1, 32, 33, 0, 2) == 0                              # L > 32: none needed
+    assert kb.kb_attn_seg_workspace_bytes(1, 32, 1, 8191, 8) == 32 * 8 * 132 * 4
+
+
 def test_packed_shape_limits(kb):
     assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 33, 0, 64, 0) == kb.KB_ERR_INVALID_ARG
     assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 4, 0, 64, -1) == kb.KB_ERR_INVALID_ARG
