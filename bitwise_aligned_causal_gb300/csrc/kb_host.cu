@@ -21,8 +21,15 @@ constexpr int kMaxDevices = 64;
 // Device error word (0 = fine).  Kernels get its address as an argument.
 __device__ uint32_t g_kb_error_word;
 
+// Library-owned scratch for kb_attn_decode_seg_static: the per-segment
+// partials of a segmented decode (132 floats per row and segment), 4 MiB,
+// one copy per device, reached through cudaGetSymbolAddress.
+constexpr size_t kSegScratchFloats = size_t(1) << 20;
+static __device__ __align__(256) float g_seg_scratch[kSegScratchFloats];
+
 struct DeviceState {
   uint32_t* err = nullptr;
+  float* seg_scratch = nullptr;   // g_seg_scratch on this device
   int sm_count = 0;
   bool ready = false;
 };
@@ -49,6 +56,8 @@ kb_status get_device_state(DeviceState** out) {
     void* p = nullptr;
     if ((e = cudaGetSymbolAddress(&p, g_kb_error_word)) != cudaSuccess) return cuda_fail(e);
     st.err = static_cast<uint32_t*>(p);
+    if ((e = cudaGetSymbolAddress(&p, g_seg_scratch)) != cudaSuccess) return cuda_fail(e);
+    st.seg_scratch = static_cast<float*>(p);
     if ((e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_fail(e);
     st.ready = true;
@@ -332,6 +341,21 @@ kb_status kb_attn_decode_seg(const void* q, const void* k, const void* v, void* 
   if (ctx_len < 1 || ctx_len > kv_cap || seg_tiles < 1) return KB_ERR_INVALID_ARG;
   return chunk_impl(q, k, v, o, B, Hq, Hkv, 1, ctx_len - 1, kv_cap, 0, stream, nullptr, nullptr, nullptr, seg_tiles,
                     workspace, workspace_bytes);
+}
+
+kb_status kb_attn_decode_seg_static(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
+                                    int ctx_len, int kv_cap, int seg_tiles, void* stream) {
+  if (ctx_len < 1 || ctx_len > kv_cap || seg_tiles < 1) return KB_ERR_INVALID_ARG;
+  const size_t need = kb_attn_seg_workspace_bytes(B, Hq, 1, ctx_len - 1, seg_tiles);
+  if (need == 0) return KB_ERR_INVALID_ARG;
+  if (need > kSegScratchFloats * sizeof(float)) return KB_ERR_UNSUPPORTED;
+  kb_status s = check_ptrs(q, k, v, o);
+  if (s != KB_OK) return s;
+  if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
+  DeviceState* dst = nullptr;
+  if ((s = get_device_state(&dst)) != KB_OK) return s;
+  return chunk_impl(q, k, v, o, B, Hq, Hkv, 1, ctx_len - 1, kv_cap, 0, stream, nullptr, nullptr, nullptr, seg_tiles,
+                    dst->seg_scratch, kSegScratchFloats * sizeof(float));
 }
 
 kb_status kb_attn_prefill_lse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,

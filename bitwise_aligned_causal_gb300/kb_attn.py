@@ -44,6 +44,7 @@ _SIGS = {
     "kb_attn_chunk_seg": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P],
     "kb_attn_decode_seg": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P],
     "kb_attn_seg_workspace_bytes": [_I, _I, _I, _I, _I],
+    "kb_attn_decode_seg_static": [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
     "kb_attn_backward": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P],
     "kb_status_string": [_I],
     "kb_contract_version": [],
@@ -142,6 +143,10 @@ def kb_attn_decode_seg(q, k, v, o, B, Hq, Hkv, ctx_len, kv_cap, seg_tiles, works
                        stream=None) -> int:
     return _lib.kb_attn_decode_seg(q, k, v, o, B, Hq, Hkv, ctx_len, kv_cap, seg_tiles, workspace, workspace_bytes,
                                    stream)
+
+
+def kb_attn_decode_seg_static(q, k, v, o, B, Hq, Hkv, ctx_len, kv_cap, seg_tiles, stream=None) -> int:
+    return _lib.kb_attn_decode_seg_static(q, k, v, o, B, Hq, Hkv, ctx_len, kv_cap, seg_tiles, stream)
 
 
 def kb_attn_seg_workspace_bytes(B, Hq, L, start, seg_tiles) -> int:
@@ -391,4 +396,17 @@ def decode_seg(q, k, v, ctx_len, seg_tiles, out=None, workspace=None, stream=Non
     _raise(kb_attn_decode_seg(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, k.shape[1],
                               int(ctx_len), k.shape[2], int(seg_tiles), ws.data_ptr(),
                               ws.numel() * ws.element_size(), _stream(stream)), "kb_attn_decode_seg")
+    return o
+
+
+def decode_seg_static(q, k, v, ctx_len, seg_tiles, out=None, stream=None):
+    """Segmented-mode decode with the library's own scratch (no workspace argument, no allocation)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, 4)
+    B, Hq = q.shape[0], q.shape[1]
+    o = _torch().empty_like(q) if out is None else out
+    _check(o, "out", 4)
+    _raise(kb_attn_decode_seg_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, k.shape[1],
+                                     int(ctx_len), k.shape[2], int(seg_tiles), _stream(stream)),
+           "kb_attn_decode_seg_static")
     return o

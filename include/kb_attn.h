@@ -188,6 +188,18 @@ kb_status kb_attn_chunk_seg(const void* q, const void* k, const void* v, void* o
 kb_status kb_attn_decode_seg(const void* q, const void* k, const void* v, void* o,
                              int B, int Hq, int Hkv, int ctx_len, int kv_cap, int seg_tiles,
                              void* workspace, size_t workspace_bytes, void* stream);
+/*
+ * kb_attn_decode_seg without a caller workspace: the partials go to a 4 MiB
+ * scratch array the library owns (one per device, part of the loaded module),
+ * so the call allocates nothing and takes nothing but the decode's tensors.
+ * Requests needing more than 4 MiB of partials (B * Hq * segments * 528 bytes)
+ * return KB_ERR_UNSUPPORTED.  The scratch is shared: calls of this entry point
+ * on one device must not overlap (issue them on one stream).  Bits equal
+ * kb_attn_decode_seg's.
+ */
+kb_status kb_attn_decode_seg_static(const void* q, const void* k, const void* v, void* o,
+                                    int B, int Hq, int Hkv, int ctx_len, int kv_cap, int seg_tiles,
+                                    void* stream);
 /* Workspace bytes kb_attn_chunk_seg / kb_attn_decode_seg need for a chunk of
  * L <= 32 rows at positions start..start+L-1 (0 for bad arguments or L > 32). */
 size_t kb_attn_seg_workspace_bytes(int B, int Hq, int L, int start, int seg_tiles);

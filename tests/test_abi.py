@@ -120,6 +120,10 @@ def test_segmented_mode_rejects_bad_arguments(kb):
     assert kb.kb_attn_decode_seg(*args, 100, 200, 2, FAKE + 8, need) == kb.KB_ERR_INVALID_ARG  # misaligned
     assert kb.kb_attn_seg_workspace_bytes(1, 32, 33, 0, 2) == 0                              # L > 32: none needed
     assert kb.kb_attn_seg_workspace_bytes(1, 32, 1, 8191, 8) == 32 * 8 * 132 * 4
+    # the static-scratch variant: 4 MiB of partials at most, checked before any CUDA call
+    assert kb.kb_attn_decode_seg_static(*args, 100, 200, 0) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_decode_seg_static(FAKE, FAKE, FAKE, FAKE, 64, 32, 8, 1 << 16, 1 << 16, 1) == \
+        kb.KB_ERR_UNSUPPORTED
 
 
 def test_packed_shape_limits(kb):
