@@ -302,10 +302,58 @@ def run_ours(args, rank, world, local):
     else:
         e2e = run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_attn)
     bwd = None if args.no_backward else run_backward(args, q, k, v, stream, world, local, rank, kb_attn)
+    seg = None if args.no_segmented else run_segmented(args, stream, world, local, rank, kb_attn)
     if rank != 0:
         return
     emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks, x,
-              bwd)
+              bwd, seg)
+
+
+SEG_DECODE_B, SEG_DECODE_CTX, SEG_TILES = 1, 8192, 4
+
+
+def run_segmented(args, stream, world, local, rank, kb_attn):
+    """Small-batch decode (B=1, ctx 8192) in the default mode and in the
+    segmented mode (segments of SEG_TILES key tiles, one CTA each), each timed
+    alone; the decode's K/V (33.6 MB) fits in L2, so a 512 MB read flushes it
+    before every timed launch."""
+    import numpy as np
+    import torch
+
+    from bitwise_aligned_causal_gb300 import inputs
+
+    y = inputs.make_qkv(SEG_DECODE_B, SEG_DECODE_CTX, SEED_DECODE + 7 + 1000 * rank, Lq=1)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(stream.device)
+
+    q, k, v = to_dev(y.q), to_dev(y.k), to_dev(y.v)
+    o = torch.empty_like(q)
+    ws = torch.empty(kb_attn.kb_attn_seg_workspace_bytes(SEG_DECODE_B, HQ, 1, SEG_DECODE_CTX - 1, SEG_TILES),
+                     dtype=torch.uint8, device=q.device)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=q.device)
+    reps = max(5, min(args.steps, 20))
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        total = 0.0
+        for _ in range(reps):
+            flush.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            total += e0.elapsed_time(e1)
+        return total / reps
+
+    barrier(world, local)
+    d_ms = timed(lambda: kb_attn.decode(q, k, v, SEG_DECODE_CTX, out=o))
+    s_ms = timed(lambda: kb_attn.decode_seg(q, k, v, SEG_DECODE_CTX, SEG_TILES, out=o, workspace=ws))
+    kb_attn.check_device_status()
+    dev = "cuda" if world > 1 else "cpu"
+    return {"default_ms": reduce_max(d_ms, world, dev), "seg_ms": reduce_max(s_ms, world, dev), "reps": reps}
 
 
 def run_backward(args, q, k, v, stream, world, local, rank, kb_attn):
@@ -447,7 +495,7 @@ def run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_att
 
 
 def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks,
-              x, bwd=None):
+              x, bwd=None, seg=None):
     pf = prefill_flops(PREFILL_B, PREFILL_S)
     db = decode_bytes(DECODE_B, DECODE_CTX)
     peaks = load_peaks()
@@ -499,6 +547,17 @@ def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_ma
         "gpu_launches": 2 * n,
         "clocks": clocks,
     }
+    if seg is not None:
+        sb = decode_bytes(SEG_DECODE_B, SEG_DECODE_CTX)
+        line["decode_small_batch"] = {
+            "workload": f"one-token decode B={SEG_DECODE_B} ctx={SEG_DECODE_CTX}, L2 flushed before each launch",
+            "default": {"value": aggregate(sb, world, seg["default_ms"] / 1e3) / 1e9, "unit": "GB/s",
+                        "us": seg["default_ms"] * 1e3},
+            "segmented": {"value": aggregate(sb, world, seg["seg_ms"] / 1e3) / 1e9, "unit": "GB/s",
+                          "us": seg["seg_ms"] * 1e3, "seg_tiles": SEG_TILES,
+                          "note": "contract C5: kb_attn_decode_seg, one CTA per (segment, b, kv head) + fold"},
+            "reps": seg["reps"],
+        }
     if bwd is not None:
         bf = 2.5 * pf                                   # dq, dk, dv: five products of the forward's size
         per_launch = bf / (bwd["bwd_ms_local"] / 1e3) / 1e12
@@ -585,6 +644,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip timing the training forward + backward")
+    ap.add_argument("--no-segmented", action="store_true", help="skip timing the small-batch segmented decode")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="full")
     ap.add_argument("--sweep", action="store_true",
                     help="time every prefill (S x B) and decode (ctx x B) configuration of the grid instead")
