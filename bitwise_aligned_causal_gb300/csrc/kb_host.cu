@@ -152,7 +152,9 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   if (L < 1 || start < 0 || kv_cap < 1) return KB_ERR_INVALID_ARG;
   if (static_cast<long long>(start) + L > kv_cap) return KB_ERR_INVALID_ARG;
   if (kv_cap > kMaxRows) return KB_ERR_UNSUPPORTED;
-  if (q_tiles_per_cta < 0 || q_tiles_per_cta > kb::kShapeOneTilePerSm) return KB_ERR_INVALID_ARG;
+  if (q_tiles_per_cta < 0 || q_tiles_per_cta > kb::kShapePersistent) return KB_ERR_INVALID_ARG;
+  const bool force_persistent = (q_tiles_per_cta == kb::kShapePersistent);
+  if (force_persistent) q_tiles_per_cta = kb::kShapeOneTilePerSm;
   if (q_tiles_per_cta == 0 && L > kb::kMaxPackedRows) return KB_ERR_INVALID_ARG;
   if (lse != nullptr && q_tiles_per_cta != kb::kShapeOneTilePerSm) return KB_ERR_INVALID_ARG;
   if (seg_tiles < 0) return KB_ERR_INVALID_ARG;
@@ -270,6 +272,13 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   a.group_major = grid > 4LL * dst->sm_count ? 1 : 0;
   a.lse = lse;
   a.seg_tiles = seg_tiles;
+  a.max_ctas = dst->sm_count > 0 ? dst->sm_count : 1;
+  if (q_tiles_per_cta == kb::kShapeOneTilePerSm) {
+    // persistent when the pairs balance: at most one per CTA, or so many
+    // that one pair more is under 3 % of a CTA's share
+    const long long pairs = static_cast<long long>((a.n_tiles + 1) / 2) * kb::kGroup * B * Hkv;
+    a.persistent = (force_persistent || pairs <= a.max_ctas || pairs >= 32LL * a.max_ctas) ? 1 : 0;
+  }
   if (ragged) {
     a.starts = ragged->starts;
     a.lens = ragged->lens;

@@ -23,6 +23,8 @@ struct PrefillArgs {
   int group_major;         // CTA order: 1 = (b, g) slowest, 0 = query tile slowest
   float* lse;              // optional [B, Hq, L] fp32: natural-log log-sum-exp of each row's scaled scores
   int seg_tiles;           // C5 segmented mode: segment length in key tiles (0 = default mode)
+  int max_ctas;            // CTAs of a persistent launch (one per SM)
+  int persistent;          // 1: CTAs walk pairs of units; 0: one CTA per unit
   uint32_t* err;    // device error word
 };
 
@@ -60,6 +62,8 @@ cudaError_t launch_prefill(int q_tiles_per_cta, const CUtensorMap& tq, const CUt
 // and separate Q K^T / P V issuers, so the tensor pipe works on later key
 // tiles while the softmax runs (CTA shape 3).
 constexpr int kShapeOneTilePerSm = 3;
+// The same kernel with the persistent launch forced (tests of the schedule).
+constexpr int kShapePersistent = 4;
 cudaError_t launch_prefill_s2(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const PrefillArgs& a, cudaStream_t s);
 // n_sub: 1, or 2 when the chunk crosses a 128-position tile boundary.

@@ -48,8 +48,11 @@ struct Prefill2Cfg {
   static constexpr int kBarSFull = kBarVFull + kStages;
   static constexpr int kBarPFull = kBarSFull + kSBufs;
   static constexpr int kBarOFull = kBarPFull + kSBufs;
-  static constexpr int kBarVReady = kBarOFull + kSBufs;    // last V tile with its tail zeroed
-  static constexpr int kBarDrain = kBarVReady + 1;         // 2: one per MMA issuer
+  // per V slot: a unit's last V tile landed there with its tail zeroed
+  static constexpr int kBarVReady = kBarOFull + kSBufs;
+  static constexpr int kBarQEmpty = kBarVReady + kStages;  // a unit's last Q K^T done: Q may be replaced
+  static constexpr int kBarOFree = kBarQEmpty + 1;         // a unit's epilogue read O (256 arrivals)
+  static constexpr int kBarDrain = kBarOFree + 1;          // 2: one per MMA issuer
   static constexpr int kNumBars = kBarDrain + 2;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemUsed = kMiscOff + 16;
@@ -61,6 +64,85 @@ __device__ __forceinline__ void drain_wait2(uint32_t bar, uint32_t parity) {
   while (!mbar_try_wait(bar, parity))
     if (global_timer_ns() - t0 > 50000000ull) break;
 }
+
+// One work unit: (b, head, absolute query tile) and its geometry.
+// Persistent launch (one CTA per SM): units come in pairs of one head's
+// query-tile ranks r and n-1-r, whose causal lengths add up to n+1 key tiles
+// whatever r is; a CTA runs pairs blockIdx.x, blockIdx.x + gridDim.x, ...,
+// so every CTA gets the same work to within one pair.  Pairs are numbered
+// (b, kv head) slowest, so the CTAs resident at one time share one GQA
+// group's K/V in L2.  Otherwise: one unit per CTA, longest first (the
+// hardware scheduler balances), group-major or query-tile-major.
+struct Unit {
+  int b, g, h, t;       // batch, kv head, query head, absolute query tile
+  int start, L;         // the sequence's first query position and row count
+  int n_kv;             // C1: key tiles 0..t
+  bool zero_tail;       // the last V tile's rows past the sequence are zeroed
+  int kv_len;
+};
+
+__device__ __forceinline__ int pairs_per_group(const PrefillArgs& args) {
+  return ((args.n_tiles + 1) / 2) * kGroup;
+}
+
+// Unit `second` (0: rank r, 1: rank n-1-r) of pair p.  False when that unit
+// does not exist (the middle rank of an odd n, or a ragged batch's shorter
+// sequence); a bad per-sequence start or length is reported and skipped.
+__device__ __forceinline__ bool unit_of(int p, int second, const PrefillArgs& args, Unit& w) {
+  int tile_rank;
+  if (args.persistent) {
+    const int ppg = pairs_per_group(args);
+    const int bg = p / ppg;
+    const int rem = p % ppg;
+    const int r = rem / kGroup;
+    tile_rank = second ? args.n_tiles - 1 - r : r;
+    if (second && tile_rank == r) return false;
+    w.b = bg / args.Hkv;
+    w.g = bg % args.Hkv;
+    w.h = w.g * kGroup + rem % kGroup;
+  } else if (args.group_major) {
+    const int units_per_group = args.n_tiles * kGroup;
+    const int bg = p / units_per_group;
+    const int rem = p % units_per_group;
+    tile_rank = rem / kGroup;
+    w.b = bg / args.Hkv;
+    w.g = bg % args.Hkv;
+    w.h = w.g * kGroup + rem % kGroup;
+  } else {
+    tile_rank = p / (args.B * args.Hq);
+    const int rem = p % (args.B * args.Hq);
+    w.b = rem / args.Hq;
+    w.h = rem % args.Hq;
+    w.g = w.h / kGroup;
+  }
+  int first_tile = args.first_tile, n_tiles = args.n_tiles;
+  w.start = args.start;
+  w.L = args.L;
+  if (args.starts != nullptr) {
+    w.start = args.starts[w.b];
+    w.L = args.lens[w.b];
+    if (w.start < 0 || w.L < 0 || w.L > args.L || w.start + w.L > args.kv_cap) {
+      if (threadIdx.x == 0 && tile_rank == 0 && (w.h % kGroup) == 0)
+        atomicCAS(args.err, 0u, static_cast<uint32_t>(kDevBadInput));
+      return false;
+    }
+    if (w.L == 0) return false;
+    first_tile = w.start / kTileRows;
+    n_tiles = (w.start + w.L - 1) / kTileRows - first_tile + 1;
+  }
+  if (tile_rank >= n_tiles) return false;
+  w.t = first_tile + n_tiles - 1 - tile_rank;
+  w.n_kv = w.t + 1;
+  w.kv_len = w.start + w.L;
+  w.zero_tail = (args.block_table != nullptr) || (args.starts != nullptr);
+  return true;
+}
+
+// Every role of a CTA walks the same units in the same order.
+#define KB_FOR_EACH_UNIT(w)                                                             \
+  for (int kb_p = blockIdx.x; kb_p < n_items; kb_p += gridDim.x)                        \
+    for (int kb_second = 0; kb_second < (args.persistent ? 2 : 1); ++kb_second)          \
+      if (Unit w; unit_of(kb_p, kb_second, args, w))
 
 template <bool kSeg>
 __global__ void __launch_bounds__(Prefill2Cfg<kSeg>::kThreads, 1)
@@ -77,46 +159,15 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // Work unit (b, h, absolute query tile t), a GQA group's four heads
-  // adjacent.  Group-major order: (b, g) slowest, so the CTAs resident at one
-  // time share one group's K/V in L2, query tiles longest first within it.
-  // Otherwise the query tile is slowest (longest first over the whole grid).
-  int b, g, h, tile_rank;
-  if (args.group_major) {
-    const int units_per_group = args.n_tiles * kGroup;
-    const int bg = blockIdx.x / units_per_group;
-    const int rem = blockIdx.x % units_per_group;
-    tile_rank = rem / kGroup;
-    b = bg / args.Hkv;
-    g = bg % args.Hkv;
-    h = g * kGroup + rem % kGroup;
-  } else {
-    tile_rank = blockIdx.x / (args.B * args.Hq);
-    const int rem = blockIdx.x % (args.B * args.Hq);
-    b = rem / args.Hq;
-    h = rem % args.Hq;
-    g = h / kGroup;
-  }
-  int start = args.start, L = args.L, first_tile = args.first_tile, n_tiles = args.n_tiles;
-  if (args.starts != nullptr) {
-    start = args.starts[b];
-    L = args.lens[b];
-    if (start < 0 || L < 0 || L > args.L || start + L > args.kv_cap) {
-      if (threadIdx.x == 0) atomicCAS(args.err, 0u, static_cast<uint32_t>(kDevBadInput));
-      return;
-    }
-    if (L == 0) return;
-    first_tile = start / kTileRows;
-    n_tiles = (start + L - 1) / kTileRows - first_tile + 1;
-  }
-  if (tile_rank >= n_tiles) return;
-  const int t = first_tile + n_tiles - 1 - tile_rank;
-  const int n_kv = t + 1;                                          // C1: KV tiles 0..t
+  const int n_items = args.persistent ? args.B * args.Hkv * pairs_per_group(args)     // pairs
+                                      : args.n_tiles * args.B * args.Hq;              // units
+  static_assert(Cfg::kSBufs == Cfg::kStages, "slot and buffer indices coincide");
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Cfg::kNumBars; ++i)
-      mbar_init(bar(i), (i >= Cfg::kBarPFull && i < Cfg::kBarPFull + Cfg::kSBufs) ? 256u : 1u);
+    for (int i = 0; i < Cfg::kNumBars; ++i) {
+      const bool warps = (i >= Cfg::kBarPFull && i < Cfg::kBarPFull + Cfg::kSBufs) || i == Cfg::kBarOFree;
+      mbar_init(bar(i), warps ? 256u : 1u);
+    }
     misc[1] = (*reinterpret_cast<volatile uint32_t*>(args.err) != 0) ? 1u : 0u;
     fence_mbar_init();
   }
@@ -129,100 +180,116 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const bool skip = (*abort_flag != 0);
-  const bool paged = args.block_table != nullptr;
-  const int kv_len = start + L;
-  const bool zero_tail = paged || (args.starts != nullptr);
+  // Every role walks the same units and counts the tiles it has handled (T)
+  // and the units (U); ring slots, S buffers and every barrier parity follow
+  // from those counts, so the CTA's units form one continuous pipeline.
 
   if (warp == Cfg::kLoadWarpK || warp == Cfg::kLoadWarpV) {
     // ----------------------------------------------------------- producers
-    // One warp per ring (K with Q; V with the tail zeroing), so that each ring
-    // runs kStages tiles ahead of its own consumer: K(j+2) is wanted right
-    // after P V(j), long before V(j+1)'s slot frees.
+    // One warp per ring (Q and K; V with the tail zeroing): each ring runs
+    // kStages tiles ahead of its consumer, across unit boundaries.
     const bool is_v = (warp == Cfg::kLoadWarpV);
     if (!skip) {
       const uint64_t keep = l2_policy_evict_last();
       const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
       const int full0 = is_v ? Cfg::kBarVFull : Cfg::kBarKFull;
-      const int empty0 = is_v ? Cfg::kBarOFull : Cfg::kBarSFull;   // slot j%3 free: P V(j) / Q K^T(j) done
+      const int empty0 = is_v ? Cfg::kBarOFull : Cfg::kBarSFull;   // slot T%3 free: P V(T) / Q K^T(T) done
       const uint32_t ring = sbase + (is_v ? Cfg::kVOff : Cfg::kKOff);
       if (lane == 0) {
         tma_prefetch_desc(tmap);
-        if (!is_v) {
-          tma_prefetch_desc(&tmap_q);
-          mbar_arrive_expect_tx(bar(Cfg::kBarQFull), kTileBytes);
-          tma_load_tile(sbase + Cfg::kQOff, &tmap_q, t * kTileRows - start, b * args.Hq + h, bar(Cfg::kBarQFull));
-        }
+        if (!is_v) tma_prefetch_desc(&tmap_q);
       }
-      int issued = 0;
+      int T = 0, U = 0, q_loads = 0;
       bool ok = true;
-      for (int j = 0; j < n_kv; ++j) {
-        const int slot = j % Cfg::kStages;
-        const uint32_t use = j / Cfg::kStages;
-        int row = j * kTileKeys, plane = b * args.Hkv + g;
-        if (paged && lane == 0) {
-          int pg = args.block_table[static_cast<size_t>(b) * args.pages_per_seq + row / args.page_size];
-          if (pg < 0 || pg >= args.num_pages) {
-            atomicCAS(args.err, 0u, static_cast<uint32_t>(kDevBadInput));
-            pg = args.num_pages;       // beyond the map: the TMA unit reads zeros
-          }
-          row = row % args.page_size;
-          plane = pg * args.Hkv + g;
-        }
-        if (j >= Cfg::kStages)
-          ok = mbar_wait(bar(empty0 + slot), (use - 1) & 1, abort_flag, args.err, kDevTimeoutSlot);
-        ok = __all_sync(0xffffffffu, ok);
+      KB_FOR_EACH_UNIT(w) {
         if (!ok) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(full0 + slot), kTileBytes);
-          tma_load_tile_hint(ring + slot * kTileBytes, tmap, row, plane, bar(full0 + slot), keep);
-        }
-        issued = j + 1;
-      }
-      if (ok && is_v && zero_tail) {
-        // V rows past kv_len in the last tile may hold anything: zero them
-        const int jl = n_kv - 1;
-        const int slot = jl % Cfg::kStages;
-        ok = mbar_wait(bar(Cfg::kBarVFull + slot), (jl / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-          uint8_t* vt = smem + Cfg::kVOff + slot * kTileBytes;
-          const int tail_from = min(kTileKeys, kv_len - jl * kTileKeys);
-          for (int idx = tail_from * 16 + lane; idx < kTileKeys * 16; idx += 32) {
-            const int vr = idx >> 4;
-            const int c = idx & 15;
-            *reinterpret_cast<uint4*>(vt + (c >> 3) * kSlabBytes + (vr >> 3) * 1024 + (vr & 7) * 128 +
-                                      (((c & 7) ^ (vr & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        const bool paged = args.block_table != nullptr;
+        if (!is_v) {
+          if (U > 0) ok = mbar_wait(bar(Cfg::kBarQEmpty), (U - 1) & 1, abort_flag, args.err, kDevTimeoutSlot);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(Cfg::kBarQFull), kTileBytes);
+            tma_load_tile(sbase + Cfg::kQOff, &tmap_q, w.t * kTileRows - w.start, w.b * args.Hq + w.h,
+                          bar(Cfg::kBarQFull));
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(Cfg::kBarVReady));
+          ++q_loads;
         }
+        for (int j = 0; j < w.n_kv; ++j, ++T) {
+          const int slot = T % Cfg::kStages;
+          int row = j * kTileKeys, plane = w.b * args.Hkv + w.g;
+          if (paged && lane == 0) {
+            int pg = args.block_table[static_cast<size_t>(w.b) * args.pages_per_seq + row / args.page_size];
+            if (pg < 0 || pg >= args.num_pages) {
+              atomicCAS(args.err, 0u, static_cast<uint32_t>(kDevBadInput));
+              pg = args.num_pages;       // beyond the map: the TMA unit reads zeros
+            }
+            row = row % args.page_size;
+            plane = pg * args.Hkv + w.g;
+          }
+          if (T >= Cfg::kStages)
+            ok = mbar_wait(bar(empty0 + slot), ((T / Cfg::kStages) - 1) & 1, abort_flag, args.err, kDevTimeoutSlot);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(full0 + slot), kTileBytes);
+            tma_load_tile_hint(ring + slot * kTileBytes, tmap, row, plane, bar(full0 + slot), keep);
+          }
+        }
+        if (ok && is_v && w.zero_tail) {
+          // V rows past kv_len in the unit's last tile may hold anything: zero them
+          const int TL = T - 1;
+          const int slot = TL % Cfg::kStages;
+          ok = mbar_wait(bar(Cfg::kBarVFull + slot), (TL / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok) {
+            uint8_t* vt = smem + Cfg::kVOff + slot * kTileBytes;
+            const int tail_from = min(kTileKeys, w.kv_len - (w.n_kv - 1) * kTileKeys);
+            for (int idx = tail_from * 16 + lane; idx < kTileKeys * 16; idx += 32) {
+              const int vr = idx >> 4;
+              const int c = idx & 15;
+              *reinterpret_cast<uint4*>(vt + (c >> 3) * kSlabBytes + (vr >> 3) * 1024 + (vr & 7) * 128 +
+                                        (((c & 7) ^ (vr & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(Cfg::kBarVReady + slot));
+          }
+        }
+        ++U;
       }
       if (!ok && lane == 0) {
-        if (!is_v) drain_wait2(bar(Cfg::kBarQFull), 0);
-        for (int x = (issued > Cfg::kStages ? issued - Cfg::kStages : 0); x < issued; ++x)
+        if (!is_v && q_loads > 0) drain_wait2(bar(Cfg::kBarQFull), (q_loads - 1) & 1);
+        for (int x = (T > Cfg::kStages ? T - Cfg::kStages : 0); x < T; ++x)
           drain_wait2(bar(full0 + x % Cfg::kStages), (x / Cfg::kStages) & 1);
       }
     }
   } else if (warp == Cfg::kMmaWarp) {
     // -------------------------------------------------------- Q K^T issuer
-    // S(j) goes to buffer j%3 once P V(j-3) has read P(j-3) there.  A second
+    // S(T) goes to buffer T%3 once P V(T-3) has read P(T-3) there.  A second
     // thread issues P V, so that the tensor pipe always has the other
-    // stream's instructions while one issuer waits on a barrier.
-    static_assert(Cfg::kSBufs == Cfg::kStages, "slot and buffer indices coincide");
+    // stream's instructions while one issuer waits on a barrier.  After a
+    // unit's last Q K^T the Q buffer is released for the next unit.
     if (lane == 0 && !skip) {
       const uint32_t q_saddr = sbase + Cfg::kQOff;
-      bool ok = mbar_wait(bar(Cfg::kBarQFull), 0, abort_flag, args.err, kDevTimeoutTma);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int sb = j % Cfg::kSBufs;
-        const uint32_t use = j / Cfg::kSBufs;
-        ok = mbar_wait(bar(Cfg::kBarKFull + sb), use & 1, abort_flag, args.err, kDevTimeoutTma);
-        if (ok && j >= Cfg::kSBufs)
-          ok = mbar_wait(bar(Cfg::kBarOFull + sb), (use - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
+      int T = 0, U = 0;
+      bool ok = true;
+      KB_FOR_EACH_UNIT(w) {
         if (!ok) break;
-        tc_fence_after();
-        issue_qk(tmem_base + sb * 128u, q_saddr, 1024u, kSlabBytes, sbase + Cfg::kKOff + sb * kTileBytes);
-        tc_commit(bar(Cfg::kBarSFull + sb));
+        ok = mbar_wait(bar(Cfg::kBarQFull), U & 1, abort_flag, args.err, kDevTimeoutTma);
+        for (int j = 0; j < w.n_kv && ok; ++j, ++T) {
+          const int sb = T % Cfg::kSBufs;
+          const uint32_t use = T / Cfg::kSBufs;
+          ok = mbar_wait(bar(Cfg::kBarKFull + sb), use & 1, abort_flag, args.err, kDevTimeoutTma);
+          if (ok && T >= Cfg::kSBufs)
+            ok = mbar_wait(bar(Cfg::kBarOFull + sb), (use - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk(tmem_base + sb * 128u, q_saddr, 1024u, kSlabBytes, sbase + Cfg::kKOff + sb * kTileBytes);
+          tc_commit(bar(Cfg::kBarSFull + sb));
+        }
+        if (ok) tc_commit(bar(Cfg::kBarQEmpty));
+        ++U;
       }
       if (!ok) {
         tc_commit(bar(Cfg::kBarDrain));
@@ -231,24 +298,37 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     }
   } else if (warp == Cfg::kPvWarp) {
     // ---------------------------------------------------------- P V issuer
+    // A unit's first P V clears O, so it waits until the previous unit's
+    // epilogue has read O.
     if (lane == 0 && !skip) {
+      int T = 0, U = 0;
+      uint32_t zero_parity = 0;                                     // bit s: zero-tail phases of V slot s, mod 2
       bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int sb = j % Cfg::kSBufs;
-        const uint32_t use = j / Cfg::kSBufs;
-        ok = mbar_wait(bar(Cfg::kBarPFull + sb), use & 1, abort_flag, args.err, kDevTimeoutSoftmax);
-        if (ok) {
-          if (zero_tail && j == n_kv - 1)
-            ok = mbar_wait(bar(Cfg::kBarVReady), 0, abort_flag, args.err, kDevTimeoutTma);
-          else
-            ok = mbar_wait(bar(Cfg::kBarVFull + sb), use & 1, abort_flag, args.err, kDevTimeoutTma);
-        }
+      KB_FOR_EACH_UNIT(w) {
         if (!ok) break;
-        tc_fence_after();
-        // the first tile (of each segment, in segmented mode) clears O
-        const bool first = kSeg ? (j % args.seg_tiles == 0) : (j == 0);
-        issue_pv(tmem_base + Cfg::kOCol, tmem_base + sb * 128u, sbase + Cfg::kVOff + sb * kTileBytes, first);
-        tc_commit(bar(Cfg::kBarOFull + sb));
+        for (int j = 0; j < w.n_kv && ok; ++j, ++T) {
+          const int sb = T % Cfg::kSBufs;
+          const uint32_t use = T / Cfg::kSBufs;
+          ok = mbar_wait(bar(Cfg::kBarPFull + sb), use & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+          if (ok) {
+            if (w.zero_tail && j == w.n_kv - 1) {
+              ok = mbar_wait(bar(Cfg::kBarVReady + sb), (zero_parity >> sb) & 1u, abort_flag, args.err,
+                             kDevTimeoutTma);
+              zero_parity ^= 1u << sb;
+            } else {
+              ok = mbar_wait(bar(Cfg::kBarVFull + sb), use & 1, abort_flag, args.err, kDevTimeoutTma);
+            }
+          }
+          if (ok && j == 0 && U > 0)
+            ok = mbar_wait(bar(Cfg::kBarOFree), (U - 1) & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+          if (!ok) break;
+          tc_fence_after();
+          // the first tile (of each segment, in segmented mode) clears O
+          const bool first = kSeg ? (j % args.seg_tiles == 0) : (j == 0);
+          issue_pv(tmem_base + Cfg::kOCol, tmem_base + sb * 128u, sbase + Cfg::kVOff + sb * kTileBytes, first);
+          tc_commit(bar(Cfg::kBarOFull + sb));
+        }
+        ++U;
       }
       if (!ok) {
         tc_commit(bar(Cfg::kBarDrain + 1));
@@ -265,160 +345,169 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     const int rB = rA + 8;
     const uint32_t o_tmem = tmem_base + Cfg::kOCol + lane_off;
     const uint32_t oacc_tmem = tmem_base + Cfg::kOAccCol + lane_off;   // segmented mode only
-    RowState sA = row_state_init();
-    RowState sB = row_state_init();
-    RowState accA = row_state_init();                               // folded segments (segmented mode)
-    RowState accB = row_state_init();
+    int T = 0;
     bool ok = !skip;
-    for (int j = 0; j < n_kv && ok; ++j) {
-      const int sb = j % Cfg::kSBufs;
-      ok = mbar_wait(bar(Cfg::kBarSFull + sb), (j / Cfg::kSBufs) & 1, abort_flag, args.err, kDevTimeoutMma);
-      ok = __all_sync(0xffffffffu, ok);
+    KB_FOR_EACH_UNIT(w) {
       if (!ok) break;
-      tc_fence_after();
-      const uint32_t s_tmem = tmem_base + sb * 128u + lane_off;
-      float xA[32], xB[32];
-      {
-        uint32_t v[32];
-        tmem_ld_16x256b_x8_wait(s_tmem, v);                         // keys 0..63
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          xA[2 * r] = __uint_as_float(v[4 * r]);
-          xA[2 * r + 1] = __uint_as_float(v[4 * r + 1]);
-          xB[2 * r] = __uint_as_float(v[4 * r + 2]);
-          xB[2 * r + 1] = __uint_as_float(v[4 * r + 3]);
-        }
-        tmem_ld_16x256b_x8_wait(s_tmem + 64u, v);                   // keys 64..127
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          xA[16 + 2 * r] = __uint_as_float(v[4 * r]);
-          xA[16 + 2 * r + 1] = __uint_as_float(v[4 * r + 1]);
-          xB[16 + 2 * r] = __uint_as_float(v[4 * r + 2]);
-          xB[16 + 2 * r + 1] = __uint_as_float(v[4 * r + 3]);
-        }
-      }
-      const bool seg_start = kSeg && (j % args.seg_tiles == 0);
-      if (seg_start) {                                              // C5: each segment starts fresh
-        sA = row_state_init();
-        sB = row_state_init();
-      }
-      uint32_t pA[16], pB[16];
-      float aA, aB;
-      if (j == n_kv - 1) {                                          // diagonal tile: causal mask
-        aA = row_softmax_tile_quad<true>(xA, u, rA + 1, sA, pA);
-        aB = row_softmax_tile_quad<true>(xB, u, rB + 1, sB, pB);
-      } else {
-        aA = row_softmax_tile_quad<false>(xA, u, kTileKeys, sA, pA);
-        aB = row_softmax_tile_quad<false>(xB, u, kTileKeys, sB, pB);
-      }
-      if (j > 0 && !seg_start && __any_sync(0xffffffffu, aA != 1.0f || aB != 1.0f)) {
-        // O must hold P V of tile j-1 before it is rescaled; per-buffer
-        // barriers keep this wait exact although it is only taken when needed
-        // (P V(j-4) is done: S(j) was committed after it)
-        ok = mbar_wait(bar(Cfg::kBarOFull + (j - 1) % Cfg::kSBufs), ((j - 1) / Cfg::kSBufs) & 1, abort_flag,
-                       args.err, kDevTimeoutMma);
+      const int n_kv = w.n_kv;
+      RowState sA = row_state_init();
+      RowState sB = row_state_init();
+      RowState accA = row_state_init();                             // folded segments (segmented mode)
+      RowState accB = row_state_init();
+      for (int j = 0; j < n_kv && ok; ++j, ++T) {
+        const int sb = T % Cfg::kSBufs;
+        ok = mbar_wait(bar(Cfg::kBarSFull + sb), (T / Cfg::kSBufs) & 1, abort_flag, args.err, kDevTimeoutMma);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t o[32];
-          tmem_ld_16x256b_x8_wait(o_tmem + 64u * half, o);
+        const uint32_t s_tmem = tmem_base + sb * 128u + lane_off;
+        float xA[32], xB[32];
+        {
+          uint32_t v[32];
+          tmem_ld_16x256b_x8_wait(s_tmem, v);                       // keys 0..63
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
-            const float2 ra = __fmul2_rn(make_float2(__uint_as_float(o[4 * r]), __uint_as_float(o[4 * r + 1])),
-                                         make_float2(aA, aA));
-            const float2 rb = __fmul2_rn(make_float2(__uint_as_float(o[4 * r + 2]), __uint_as_float(o[4 * r + 3])),
-                                         make_float2(aB, aB));
-            o[4 * r] = __float_as_uint(ra.x);
-            o[4 * r + 1] = __float_as_uint(ra.y);
-            o[4 * r + 2] = __float_as_uint(rb.x);
-            o[4 * r + 3] = __float_as_uint(rb.y);
+            xA[2 * r] = __uint_as_float(v[4 * r]);
+            xA[2 * r + 1] = __uint_as_float(v[4 * r + 1]);
+            xB[2 * r] = __uint_as_float(v[4 * r + 2]);
+            xB[2 * r + 1] = __uint_as_float(v[4 * r + 3]);
           }
-          tmem_st_16x256b_x8(o_tmem + 64u * half, o);
-        }
-      }
-      {
-        uint32_t pv[32];
+          tmem_ld_16x256b_x8_wait(s_tmem + 64u, v);                 // keys 64..127
 #pragma unroll
-        for (int r = 0; r < 16; ++r) { pv[2 * r] = pA[r]; pv[2 * r + 1] = pB[r]; }
-        tmem_st_16x128b_x16(s_tmem, pv);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(Cfg::kBarPFull + sb));
-      if constexpr (kSeg) {
-        if (j % args.seg_tiles == args.seg_tiles - 1 || j == n_kv - 1) {
-          // C5: the segment ends here; fold its (m, mc, l, O) into the
-          // accumulated segments once its last P V has finished
-          ok = mbar_wait(bar(Cfg::kBarOFull + sb), (j / Cfg::kSBufs) & 1, abort_flag, args.err, kDevTimeoutMma);
+          for (int r = 0; r < 8; ++r) {
+            xA[16 + 2 * r] = __uint_as_float(v[4 * r]);
+            xA[16 + 2 * r + 1] = __uint_as_float(v[4 * r + 1]);
+            xB[16 + 2 * r] = __uint_as_float(v[4 * r + 2]);
+            xB[16 + 2 * r + 1] = __uint_as_float(v[4 * r + 3]);
+          }
+        }
+        const bool seg_start = kSeg && (j % args.seg_tiles == 0);
+        if (seg_start) {                                            // C5: each segment starts fresh
+          sA = row_state_init();
+          sB = row_state_init();
+        }
+        uint32_t pA[16], pB[16];
+        float aA, aB;
+        if (j == n_kv - 1) {                                        // diagonal tile: causal mask
+          aA = row_softmax_tile_quad<true>(xA, u, rA + 1, sA, pA);
+          aB = row_softmax_tile_quad<true>(xB, u, rB + 1, sB, pB);
+        } else {
+          aA = row_softmax_tile_quad<false>(xA, u, kTileKeys, sA, pA);
+          aB = row_softmax_tile_quad<false>(xB, u, kTileKeys, sB, pB);
+        }
+        if (j > 0 && !seg_start && __any_sync(0xffffffffu, aA != 1.0f || aB != 1.0f)) {
+          // O must hold P V of tile T-1 before it is rescaled; per-buffer
+          // barriers keep this wait exact although it is only taken when
+          // needed (P V(T-4) is done: S(T) was committed after it)
+          ok = mbar_wait(bar(Cfg::kBarOFull + (T - 1) % Cfg::kSBufs), ((T - 1) / Cfg::kSBufs) & 1, abort_flag,
+                         args.err, kDevTimeoutMma);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
-          const bool first_seg = j < args.seg_tiles;
-          FoldScale fA{1.0f, 1.0f}, fB{1.0f, 1.0f};
-          if (first_seg) {
-            accA = sA;
-            accB = sB;
-          } else {
-            fA = fold_state(accA, sA);
-            fB = fold_state(accB, sB);
-          }
 #pragma unroll 1
           for (int half = 0; half < 2; ++half) {
-            uint32_t os[32], oa[32];
-            tmem_ld_16x256b_x8_wait(o_tmem + 64u * half, os);
+            uint32_t o[32];
+            tmem_ld_16x256b_x8_wait(o_tmem + 64u * half, o);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              const float2 ra = __fmul2_rn(make_float2(__uint_as_float(o[4 * r]), __uint_as_float(o[4 * r + 1])),
+                                           make_float2(aA, aA));
+              const float2 rb = __fmul2_rn(make_float2(__uint_as_float(o[4 * r + 2]), __uint_as_float(o[4 * r + 3])),
+                                           make_float2(aB, aB));
+              o[4 * r] = __float_as_uint(ra.x);
+              o[4 * r + 1] = __float_as_uint(ra.y);
+              o[4 * r + 2] = __float_as_uint(rb.x);
+              o[4 * r + 3] = __float_as_uint(rb.y);
+            }
+            tmem_st_16x256b_x8(o_tmem + 64u * half, o);
+          }
+        }
+        {
+          uint32_t pv[32];
+#pragma unroll
+          for (int r = 0; r < 16; ++r) { pv[2 * r] = pA[r]; pv[2 * r + 1] = pB[r]; }
+          tmem_st_16x128b_x16(s_tmem, pv);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(Cfg::kBarPFull + sb));
+        if constexpr (kSeg) {
+          if (j % args.seg_tiles == args.seg_tiles - 1 || j == n_kv - 1) {
+            // C5: the segment ends here; fold its (m, mc, l, O) into the
+            // accumulated segments once its last P V has finished
+            ok = mbar_wait(bar(Cfg::kBarOFull + sb), (T / Cfg::kSBufs) & 1, abort_flag, args.err, kDevTimeoutMma);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const bool first_seg = j < args.seg_tiles;
+            FoldScale fA{1.0f, 1.0f}, fB{1.0f, 1.0f};
             if (first_seg) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) oa[i] = os[i];
+              accA = sA;
+              accB = sB;
             } else {
-              tmem_ld_16x256b_x8_wait(oacc_tmem + 64u * half, oa);
+              fA = fold_state(accA, sA);
+              fB = fold_state(accB, sB);
+            }
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+              uint32_t os[32], oa[32];
+              tmem_ld_16x256b_x8_wait(o_tmem + 64u * half, os);
+              if (first_seg) {
 #pragma unroll
-              for (int r = 0; r < 8; ++r) {
+                for (int i = 0; i < 32; ++i) oa[i] = os[i];
+              } else {
+                tmem_ld_16x256b_x8_wait(oacc_tmem + 64u * half, oa);
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  oa[4 * r + e] = __float_as_uint(fold_o(__uint_as_float(oa[4 * r + e]),
-                                                         __uint_as_float(os[4 * r + e]), fA));
-                  oa[4 * r + 2 + e] = __float_as_uint(fold_o(__uint_as_float(oa[4 * r + 2 + e]),
-                                                             __uint_as_float(os[4 * r + 2 + e]), fB));
+                for (int r = 0; r < 8; ++r) {
+#pragma unroll
+                  for (int e = 0; e < 2; ++e) {
+                    oa[4 * r + e] = __float_as_uint(fold_o(__uint_as_float(oa[4 * r + e]),
+                                                           __uint_as_float(os[4 * r + e]), fA));
+                    oa[4 * r + 2 + e] = __float_as_uint(fold_o(__uint_as_float(oa[4 * r + 2 + e]),
+                                                               __uint_as_float(os[4 * r + 2 + e]), fB));
+                  }
                 }
               }
+              tmem_st_16x256b_x8(oacc_tmem + 64u * half, oa);
             }
-            tmem_st_16x256b_x8(oacc_tmem + 64u * half, oa);
+            tmem_st_wait();
           }
-          tmem_st_wait();
         }
       }
-    }
-    if (ok)
-      ok = mbar_wait(bar(Cfg::kBarOFull + (n_kv - 1) % Cfg::kSBufs), ((n_kv - 1) / Cfg::kSBufs) & 1, abort_flag,
-                     args.err, kDevTimeoutMma);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+      if (ok)
+        ok = mbar_wait(bar(Cfg::kBarOFull + (T - 1) % Cfg::kSBufs), ((T - 1) / Cfg::kSBufs) & 1, abort_flag,
+                       args.err, kDevTimeoutMma);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
       tc_fence_after();
       const float invA = row_inv_l(kSeg ? accA : sA);
       const float invB = row_inv_l(kSeg ? accB : sB);
       const uint32_t o_out = kSeg ? oacc_tmem : o_tmem;
-      const int iA = t * kTileRows + rA - start;                     // query row index in q / o
+      const int iA = w.t * kTileRows + rA - w.start;                 // query row index in q / o
       const int iB = iA + 8;
-      const bool stA = (iA >= 0) && (iA < L);
-      const bool stB = (iB >= 0) && (iB < L);
+      const bool stA = (iA >= 0) && (iA < w.L);
+      const bool stB = (iB >= 0) && (iB < w.L);
       if (!kSeg && args.lse != nullptr && u == 0) {
         // natural-log log-sum-exp of the row's scaled scores: the weights are
         // 2^(s c - mc), so log2 sum_j 2^(s_j c) = mc + log2(l)
         constexpr float kLn2 = 0.69314718055994531f;
-        float* lrow = args.lse + (static_cast<size_t>(b) * args.Hq + h) * static_cast<size_t>(args.L);
+        float* lrow = args.lse + (static_cast<size_t>(w.b) * args.Hq + w.h) * static_cast<size_t>(args.L);
         if (stA) lrow[iA] = __fmul_rn(__fadd_rn(sA.mc, log2f(sA.l)), kLn2);
         if (stB) lrow[iB] = __fmul_rn(__fadd_rn(sB.mc, log2f(sB.l)), kLn2);
       }
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.o) + (static_cast<size_t>(b) * args.Hq + h) *
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.o) + (static_cast<size_t>(w.b) * args.Hq + w.h) *
                                                                        static_cast<size_t>(args.L) * kHeadDim;
       uint32_t* dA = reinterpret_cast<uint32_t*>(orow + static_cast<size_t>(stA ? iA : 0) * kHeadDim);
       uint32_t* dB = reinterpret_cast<uint32_t*>(orow + static_cast<size_t>(stB ? iB : 0) * kHeadDim);
-#pragma unroll 1
+      uint32_t o0[32], o1[32];
+      tmem_ld_16x256b_x8_wait(o_out, o0);
+      tmem_ld_16x256b_x8_wait(o_out + 64u, o1);
+      // O is in registers: the next unit's first P V may clear it
+      tc_fence_before();
+      mbar_arrive(bar(Cfg::kBarOFree));
+#pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t o[32];
-        tmem_ld_16x256b_x8_wait(o_out + 64u * half, o);
+        const uint32_t* o = half ? o1 : o0;
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           const int col = 64 * half + 8 * r + 2 * u;                 // this thread's two columns
@@ -457,7 +546,11 @@ static cudaError_t launch_prefill_s2_t(const CUtensorMap& tq, const CUtensorMap&
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const long long grid = static_cast<long long>(a.n_tiles) * a.B * a.Hq;
+  // persistent: one CTA per SM at most, each walking its share of the unit
+  // pairs; otherwise one CTA per unit
+  const long long pairs = static_cast<long long>((a.n_tiles + 1) / 2) * kGroup * a.B * a.Hkv;
+  const long long grid = a.persistent ? (pairs < a.max_ctas ? pairs : a.max_ctas)
+                                      : static_cast<long long>(a.n_tiles) * a.B * a.Hq;
   kb_prefill_kernel_s2<kSeg><<<static_cast<unsigned>(grid), Cfg::kThreads, Cfg::kSmemBytes, s>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }

@@ -245,7 +245,9 @@ kb_status kb_attn_backward(const void* q, const void* k, const void* v, const vo
  * q_tiles_per_cta = 1 or 2 runs the tile kernel with that many 128-row query
  * tiles per CTA; 3 runs the tile kernel with one query tile per CTA, one CTA
  * per SM and three score buffers (Q K^T of later key tiles overlaps the
- * softmax of the current one); 0 runs the packed kernel (the 4 heads of a GQA group times
+ * softmax of the current one), launched persistent (CTAs walk balanced pairs
+ * of query tiles) or one CTA per tile as the sizes suit; 4 is 3 with the
+ * persistent launch forced; 0 runs the packed kernel (the 4 heads of a GQA group times
  * the chunk's rows in one MMA tile; L <= 32).  kb_attn_chunk, kb_attn_prefill
  * and kb_attn_decode pick packed for L <= 32 and 3 otherwise.  Every shape
  * gives the same bits.

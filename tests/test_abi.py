@@ -75,7 +75,7 @@ def test_bad_sizes_rejected(kb):
     # decode context within the cache
     assert kb.kb_attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 11, 10) == kb.KB_ERR_INVALID_ARG
     assert kb.kb_attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 0, 10) == kb.KB_ERR_INVALID_ARG
-    assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 4, 0, 10, 4) == kb.KB_ERR_INVALID_ARG
+    assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 4, 0, 10, 5) == kb.KB_ERR_INVALID_ARG
     assert kb.kb_attn_debug_wait_timeout(0) == kb.KB_ERR_INVALID_ARG
 
 

@@ -121,9 +121,11 @@ def test_cta_shapes_give_identical_bits(kb, S):
     a = from_dev(kb.chunk(q, k, v, 0, q_tiles_per_cta=1))
     b = from_dev(kb.chunk(q, k, v, 0, q_tiles_per_cta=2))
     c = from_dev(kb.chunk(q, k, v, 0, q_tiles_per_cta=3))
+    d = from_dev(kb.chunk(q, k, v, 0, q_tiles_per_cta=4))          # persistent launch forced
     kb.check_device_status()
     assert np.array_equal(a, b)
     assert np.array_equal(a, c)
+    assert np.array_equal(a, d)
 
 
 def test_repeat_runs_are_identical(kb):

@@ -77,6 +77,32 @@ def test_ragged_equals_each_sequence_alone(kb, starts, lens, L_max, cap):
         assert np.all(out[b, :, lens[b]:] == out[b, 0, L_max - 1, 0] if lens[b] < L_max else True)
 
 
+def test_ragged_persistent_launch(kb):
+    """With 8 query heads the default kernel's persistent launch (CTAs walking
+    pairs of query tiles) runs this ragged batch, whose shorter sequences
+    leave holes in the pair schedule; each sequence must still give the bits
+    of the two-CTA tile kernel run on it alone."""
+    import torch
+
+    starts, lens, L_max, cap = [0, 129, 700, 3], [300, 200, 124, 1], 300, 1000
+    B, Hkv = len(starts), 2
+    x = inputs.make_qkv(B, cap, seed=80_500, Hq=4 * Hkv, Hkv=Hkv, Lq=L_max)
+    q, k, v = to_dev(x.q), to_dev(x.k), to_dev(x.v)
+    for b in range(B):
+        q[b, :, lens[b]:] = float("nan")
+        k[b, :, starts[b] + lens[b]:] = float("nan")
+        v[b, :, starts[b] + lens[b]:] = float("nan")
+    st = torch.tensor(starts, dtype=torch.int32, device="cuda")
+    ln = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = from_dev(kb.chunk_varlen(q, k, v, st, ln))
+    for b in range(B):
+        e = starts[b] + lens[b]
+        ref = from_dev(kb.chunk(q[b:b + 1, :, :lens[b]].contiguous(), k[b:b + 1, :, :e].contiguous(),
+                                v[b:b + 1, :, :e].contiguous(), starts[b], q_tiles_per_cta=1))
+        assert np.array_equal(out[b:b + 1, :, :lens[b]], ref), b
+    kb.check_device_status()
+
+
 def test_ragged_paged(kb):
     import torch
 
