@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -274,10 +275,20 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   a.seg_tiles = seg_tiles;
   a.max_ctas = dst->sm_count > 0 ? dst->sm_count : 1;
   if (q_tiles_per_cta == kb::kShapeOneTilePerSm) {
-    // persistent when the pairs balance: at most one per CTA, or so many
-    // that one pair more is under 3 % of a CTA's share
+    // Persistent when what it saves beats what it costs: it hides a CTA's
+    // start and end (about 3000 cycles) under the previous unit, against a
+    // unit of (n+1)/2 key tiles at about 1550 cycles each; its static split
+    // leaves a tail of (ceil(p) - p) / p with p pairs per CTA, where the
+    // one-CTA-per-tile launch ends on the shortest tiles.
     const long long pairs = static_cast<long long>((a.n_tiles + 1) / 2) * kb::kGroup * B * Hkv;
-    a.persistent = (force_persistent || pairs <= a.max_ctas || pairs >= 32LL * a.max_ctas) ? 1 : 0;
+    bool persistent = pairs <= a.max_ctas;
+    if (!persistent) {
+      const double p = static_cast<double>(pairs) / a.max_ctas;
+      const double tail = (std::ceil(p) - p) / p;
+      const double saved = 3000.0 / (0.5 * (a.n_tiles + 1) * 1550.0 + 3000.0);
+      persistent = saved > tail;
+    }
+    a.persistent = (force_persistent || persistent) ? 1 : 0;
   }
   if (ragged) {
     a.starts = ragged->starts;

@@ -211,8 +211,8 @@ size_t kb_attn_seg_workspace_bytes(int B, int Hq, int L, int start, int seg_tile
  *   q, o, k, v : as kb_attn_prefill; o gets the same bits as kb_attn_prefill
  *   lse        : [B, Hq, S] fp32, device, 4-byte aligned, caller-owned;
  *                lse[b,h,i] = ln sum_{j<=i} exp(q_i . k_j / sqrt(128))
- * Always runs the one-query-tile-per-CTA kernel (CTA shape 3), whose bits
- * every other shape reproduces.
+ * Always runs the default tile kernel (CTA shape 3), whose bits every other
+ * shape reproduces.
  */
 kb_status kb_attn_prefill_lse(const void* q, const void* k, const void* v, void* o, float* lse,
                               int B, int Hq, int Hkv, int S, void* stream);
