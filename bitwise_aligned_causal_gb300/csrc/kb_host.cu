@@ -276,16 +276,17 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   a.max_ctas = dst->sm_count > 0 ? dst->sm_count : 1;
   if (q_tiles_per_cta == kb::kShapeOneTilePerSm) {
     // Persistent when what it saves beats what it costs: it hides a CTA's
-    // start and end (about 3000 cycles) under the previous unit, against a
-    // unit of (n+1)/2 key tiles at about 1550 cycles each; its static split
-    // leaves a tail of (ceil(p) - p) / p with p pairs per CTA, where the
-    // one-CTA-per-tile launch ends on the shortest tiles.
+    // start and end (about 5000 cycles, fitted to timings of both launches
+    // from S=1.5K to 16K) under the previous unit, against a unit of (n+1)/2
+    // key tiles at about 1550 cycles each; its static split leaves a tail of
+    // (ceil(p) - p) / p with p pairs per CTA, where the one-CTA-per-tile
+    // launch ends on the shortest tiles.
     const long long pairs = static_cast<long long>((a.n_tiles + 1) / 2) * kb::kGroup * B * Hkv;
     bool persistent = pairs <= a.max_ctas;
     if (!persistent) {
       const double p = static_cast<double>(pairs) / a.max_ctas;
       const double tail = (std::ceil(p) - p) / p;
-      const double saved = 3000.0 / (0.5 * (a.n_tiles + 1) * 1550.0 + 3000.0);
+      const double saved = 5000.0 / (0.5 * (a.n_tiles + 1) * 1550.0 + 5000.0);
       persistent = saved > tail;
     }
     a.persistent = (force_persistent || persistent) ? 1 : 0;
