@@ -44,7 +44,7 @@ def workload_name():
             f"Hq={HQ} Hkv={HKV} D={D} bf16")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # ncu dram bytes per launch for the current kernels (profiles/ summaries); None = not captured
-NCU_TRAFFIC_BYTES = {"prefill": 1309.5e6, "decode": 537.19e6}
+NCU_TRAFFIC_BYTES = {"prefill": 1309.8e6, "decode": 537.19e6}
 
 
 def prefill_flops(B: int, S: int) -> int:

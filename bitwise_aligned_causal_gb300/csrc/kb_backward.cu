@@ -278,8 +278,8 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t sv[32], pv[32];
-        tmem_ld_16x256b_x8_wait(tmem_base + Cfg::kColS + lane_off + 64u * half, sv);
-        tmem_ld_16x256b_x8_wait(tmem_base + Cfg::kColDP + lane_off + 64u * half, pv);
+        tmem_ld_16x256b_x8_pair_wait(tmem_base + Cfg::kColS + lane_off + 64u * half,
+                                     tmem_base + Cfg::kColDP + lane_off + 64u * half, sv, pv);
         if (half == 1) {
           tc_fence_before();
           mbar_arrive(bar(Cfg::kBarSFree));                          // S(j), dP(j) fully read
@@ -534,8 +534,8 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t sv[32], pv[32];
-        tmem_ld_16x256b_x8_wait(tmem_base + Cfg::kColST + lane_off + 64u * half, sv);
-        tmem_ld_16x256b_x8_wait(tmem_base + Cfg::kColDPT + lane_off + 64u * half, pv);
+        tmem_ld_16x256b_x8_pair_wait(tmem_base + Cfg::kColST + lane_off + 64u * half,
+                                     tmem_base + Cfg::kColDPT + lane_off + 64u * half, sv, pv);
         uint32_t pp[16], dd[16];
 #pragma unroll
         for (int r = 0; r < 8; ++r) {

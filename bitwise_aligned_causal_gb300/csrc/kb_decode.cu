@@ -407,15 +407,14 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       const uint32_t s_tmem = tmem_base + (j % Cfg::kSBufs) * 128u;
       float x[32];
       {
-        uint32_t v[32];
-        tmem_ld_16x256b_x8_wait(s_tmem, v);            // keys 0..63
-#pragma unroll
-        for (int q = 0; q < 8; ++q) { x[2 * q] = __uint_as_float(v[4 * q]); x[2 * q + 1] = __uint_as_float(v[4 * q + 1]); }
-        tmem_ld_16x256b_x8_wait(s_tmem + 64u, v);      // keys 64..127
+        uint32_t v0[32], v1[32];
+        tmem_ld_16x256b_x8_pair_wait(s_tmem, s_tmem + 64u, v0, v1);   // keys 0..63, 64..127
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          x[16 + 2 * q] = __uint_as_float(v[4 * q]);
-          x[16 + 2 * q + 1] = __uint_as_float(v[4 * q + 1]);
+          x[2 * q] = __uint_as_float(v0[4 * q]);
+          x[2 * q + 1] = __uint_as_float(v0[4 * q + 1]);
+          x[16 + 2 * q] = __uint_as_float(v1[4 * q]);
+          x[16 + 2 * q + 1] = __uint_as_float(v1[4 * q + 1]);
         }
       }
       uint32_t p[16];

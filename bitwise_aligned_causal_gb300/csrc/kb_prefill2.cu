@@ -363,22 +363,18 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         const uint32_t s_tmem = tmem_base + sb * 128u + lane_off;
         float xA[32], xB[32];
         {
-          uint32_t v[32];
-          tmem_ld_16x256b_x8_wait(s_tmem, v);                       // keys 0..63
+          uint32_t v0[32], v1[32];
+          tmem_ld_16x256b_x8_pair_wait(s_tmem, s_tmem + 64u, v0, v1);   // keys 0..63, 64..127
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
-            xA[2 * r] = __uint_as_float(v[4 * r]);
-            xA[2 * r + 1] = __uint_as_float(v[4 * r + 1]);
-            xB[2 * r] = __uint_as_float(v[4 * r + 2]);
-            xB[2 * r + 1] = __uint_as_float(v[4 * r + 3]);
-          }
-          tmem_ld_16x256b_x8_wait(s_tmem + 64u, v);                 // keys 64..127
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            xA[16 + 2 * r] = __uint_as_float(v[4 * r]);
-            xA[16 + 2 * r + 1] = __uint_as_float(v[4 * r + 1]);
-            xB[16 + 2 * r] = __uint_as_float(v[4 * r + 2]);
-            xB[16 + 2 * r + 1] = __uint_as_float(v[4 * r + 3]);
+            xA[2 * r] = __uint_as_float(v0[4 * r]);
+            xA[2 * r + 1] = __uint_as_float(v0[4 * r + 1]);
+            xB[2 * r] = __uint_as_float(v0[4 * r + 2]);
+            xB[2 * r + 1] = __uint_as_float(v0[4 * r + 3]);
+            xA[16 + 2 * r] = __uint_as_float(v1[4 * r]);
+            xA[16 + 2 * r + 1] = __uint_as_float(v1[4 * r + 1]);
+            xB[16 + 2 * r] = __uint_as_float(v1[4 * r + 2]);
+            xB[16 + 2 * r + 1] = __uint_as_float(v1[4 * r + 3]);
           }
         }
         const bool seg_start = kSeg && (j % args.seg_tiles == 0);
@@ -500,8 +496,7 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       uint32_t* dA = reinterpret_cast<uint32_t*>(orow + static_cast<size_t>(stA ? iA : 0) * kHeadDim);
       uint32_t* dB = reinterpret_cast<uint32_t*>(orow + static_cast<size_t>(stB ? iB : 0) * kHeadDim);
       uint32_t o0[32], o1[32];
-      tmem_ld_16x256b_x8_wait(o_out, o0);
-      tmem_ld_16x256b_x8_wait(o_out + 64u, o1);
+      tmem_ld_16x256b_x8_pair_wait(o_out, o_out + 64u, o0, o1);
       // O is in registers: the next unit's first P V may clear it
       tc_fence_before();
       mbar_arrive(bar(Cfg::kBarOFree));
