@@ -160,7 +160,7 @@ kb_status kb_attn_check_device_status(void* stream);
 kb_status kb_attn_debug_wait_timeout(int limit_us, void* stream);
 
 /*
- * Segmented mode (contract C5; SURVEY's fixed-segment split of the KV range):
+ * Segmented mode (contract C5: a fixed, length-determined split of the KV range):
  * a row's key tiles are cut into segments of seg_tiles 128-key tiles anchored
  * at key 0; each segment runs the default mode's tile steps from the fresh
  * state and the segments are folded left to right by one fold function, then
