@@ -275,15 +275,18 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       tc_fence_after();
       const bool diag = (j == n_kv - 1);
       uint32_t ds[32];
+      // all of S(j) and dP(j) into registers first, so S(j+1), dP(j+1) can be
+      // issued while this tile's dS is computed
+      uint32_t sv0[32], pv0[32], sv1[32], pv1[32];
+      tmem_ld_16x256b_x8_quad_wait(tmem_base + Cfg::kColS + lane_off, tmem_base + Cfg::kColDP + lane_off,
+                                   tmem_base + Cfg::kColS + lane_off + 64u, tmem_base + Cfg::kColDP + lane_off + 64u,
+                                   sv0, pv0, sv1, pv1);
+      tc_fence_before();
+      mbar_arrive(bar(Cfg::kBarSFree));                              // S(j), dP(j) fully read
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t sv[32], pv[32];
-        tmem_ld_16x256b_x8_pair_wait(tmem_base + Cfg::kColS + lane_off + 64u * half,
-                                     tmem_base + Cfg::kColDP + lane_off + 64u * half, sv, pv);
-        if (half == 1) {
-          tc_fence_before();
-          mbar_arrive(bar(Cfg::kBarSFree));                          // S(j), dP(j) fully read
-        }
+        const uint32_t* sv = half ? sv1 : sv0;
+        const uint32_t* pv = half ? pv1 : pv0;
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           float dsA[2], dsB[2];

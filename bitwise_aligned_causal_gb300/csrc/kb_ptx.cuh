@@ -357,6 +357,44 @@ __device__ __forceinline__ void tmem_ld_16x256b_x8_pair_wait(uint32_t ta, uint32
       : "memory");
 }
 
+// Four 16x256b.x8 loads under one wait.
+__device__ __forceinline__ void tmem_ld_16x256b_x8_quad_wait(uint32_t ta, uint32_t tb, uint32_t tc, uint32_t td,
+                                                            uint32_t (&ra)[32], uint32_t (&rb)[32],
+                                                            uint32_t (&rc)[32], uint32_t (&rd)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+      "{%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+      "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(ra[0]), "=r"(ra[1]), "=r"(ra[2]), "=r"(ra[3]), "=r"(ra[4]), "=r"(ra[5]), "=r"(ra[6]), "=r"(ra[7]),
+        "=r"(ra[8]), "=r"(ra[9]), "=r"(ra[10]), "=r"(ra[11]), "=r"(ra[12]), "=r"(ra[13]), "=r"(ra[14]), "=r"(ra[15]),
+        "=r"(ra[16]), "=r"(ra[17]), "=r"(ra[18]), "=r"(ra[19]), "=r"(ra[20]), "=r"(ra[21]), "=r"(ra[22]), "=r"(ra[23]),
+        "=r"(ra[24]), "=r"(ra[25]), "=r"(ra[26]), "=r"(ra[27]), "=r"(ra[28]), "=r"(ra[29]), "=r"(ra[30]), "=r"(ra[31]),
+        "=r"(rb[0]), "=r"(rb[1]), "=r"(rb[2]), "=r"(rb[3]), "=r"(rb[4]), "=r"(rb[5]), "=r"(rb[6]), "=r"(rb[7]),
+        "=r"(rb[8]), "=r"(rb[9]), "=r"(rb[10]), "=r"(rb[11]), "=r"(rb[12]), "=r"(rb[13]), "=r"(rb[14]), "=r"(rb[15]),
+        "=r"(rb[16]), "=r"(rb[17]), "=r"(rb[18]), "=r"(rb[19]), "=r"(rb[20]), "=r"(rb[21]), "=r"(rb[22]), "=r"(rb[23]),
+        "=r"(rb[24]), "=r"(rb[25]), "=r"(rb[26]), "=r"(rb[27]), "=r"(rb[28]), "=r"(rb[29]), "=r"(rb[30]), "=r"(rb[31]),
+        "=r"(rc[0]), "=r"(rc[1]), "=r"(rc[2]), "=r"(rc[3]), "=r"(rc[4]), "=r"(rc[5]), "=r"(rc[6]), "=r"(rc[7]),
+        "=r"(rc[8]), "=r"(rc[9]), "=r"(rc[10]), "=r"(rc[11]), "=r"(rc[12]), "=r"(rc[13]), "=r"(rc[14]), "=r"(rc[15]),
+        "=r"(rc[16]), "=r"(rc[17]), "=r"(rc[18]), "=r"(rc[19]), "=r"(rc[20]), "=r"(rc[21]), "=r"(rc[22]), "=r"(rc[23]),
+        "=r"(rc[24]), "=r"(rc[25]), "=r"(rc[26]), "=r"(rc[27]), "=r"(rc[28]), "=r"(rc[29]), "=r"(rc[30]), "=r"(rc[31]),
+        "=r"(rd[0]), "=r"(rd[1]), "=r"(rd[2]), "=r"(rd[3]), "=r"(rd[4]), "=r"(rd[5]), "=r"(rd[6]), "=r"(rd[7]),
+        "=r"(rd[8]), "=r"(rd[9]), "=r"(rd[10]), "=r"(rd[11]), "=r"(rd[12]), "=r"(rd[13]), "=r"(rd[14]), "=r"(rd[15]),
+        "=r"(rd[16]), "=r"(rd[17]), "=r"(rd[18]), "=r"(rd[19]), "=r"(rd[20]), "=r"(rd[21]), "=r"(rd[22]), "=r"(rd[23]),
+        "=r"(rd[24]), "=r"(rd[25]), "=r"(rd[26]), "=r"(rd[27]), "=r"(rd[28]), "=r"(rd[29]), "=r"(rd[30]), "=r"(rd[31])
+      : "r"(ta), "r"(tb), "r"(tc), "r"(td)
+      : "memory");
+}
+
 // 16x256b shape, 8 repetitions (the store of the load above).
 #define KB_V8(b) "r"(v[b + 0]), "r"(v[b + 1]), "r"(v[b + 2]), "r"(v[b + 3]), \
                  "r"(v[b + 4]), "r"(v[b + 5]), "r"(v[b + 6]), "r"(v[b + 7])
