@@ -43,8 +43,40 @@ def workload_name():
     return (f"causal GQA prefill B={PREFILL_B} S={PREFILL_S} + one-token decode B={DECODE_B} ctx={DECODE_CTX}, "
             f"Hq={HQ} Hkv={HKV} D={D} bf16")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# ncu dram bytes per launch for the current kernels (profiles/ summaries); None = not captured
-NCU_TRAFFIC_BYTES = {"prefill": 1309.8e6, "decode": 537.19e6}
+# ncu dram bytes (read + write) per launch, each with the hash of the kernel
+# sources it was captured on and the profile summary that records it.  When
+# the sources differ from that hash, the figure no longer describes the timed
+# build and the bench line reports traffic as null.
+NCU_TRAFFIC = {
+    "prefill": {"bytes": None, "sources": None, "profile": "profiles/launch_list_bench_full.md"},
+    "decode": {"bytes": None, "sources": None, "profile": "profiles/launch_list_bench_full.md"},
+}
+KERNEL_SOURCES = {
+    "prefill": ["kb_prefill2.cu", "kb_contract.cuh", "kb_ptx.cuh", "kb_launch.h", "kb_host.cu"],
+    "decode": ["kb_decode.cu", "kb_contract.cuh", "kb_ptx.cuh", "kb_launch.h", "kb_host.cu"],
+}
+
+
+def sources_hash(kernel: str) -> str:
+    """sha256 (16 hex digits) over the CUDA sources that define a kernel and its launch."""
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bitwise_aligned_causal_gb300", "csrc")
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(name.encode())
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic(kernel: str):
+    """(bytes or None, provenance dict) of the ncu DRAM traffic for the current sources."""
+    rec = NCU_TRAFFIC[kernel]
+    cur = sources_hash(kernel)
+    fresh = rec["bytes"] is not None and rec["sources"] == cur
+    return (rec["bytes"] if fresh else None), {"profile": rec["profile"], "captured_on_sources": rec["sources"],
+                                               "current_sources": cur, "fresh": fresh}
 
 
 def prefill_flops(B: int, S: int) -> int:
@@ -303,10 +335,14 @@ def run_ours(args, rank, world, local):
         e2e = run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_attn)
     bwd = None if args.no_backward else run_backward(args, q, k, v, stream, world, local, rank, kb_attn)
     seg = None if args.no_segmented else run_segmented(args, stream, world, local, rank, kb_attn)
+    grid = None
+    if not args.no_grid:
+        barrier(world, local)
+        grid = grid_summary(time_grid(kb_attn, load_peaks(), (1,), 5, dev), load_peaks())
     if rank != 0:
         return
     emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks, x,
-              bwd, seg)
+              bwd, seg, grid)
 
 
 SEG_DECODE_B, SEG_DECODE_CTX, SEG_TILES = 1, 8192, 4
@@ -495,7 +531,7 @@ def run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_att
 
 
 def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks,
-              x, bwd=None, seg=None):
+              x, bwd=None, seg=None, grid=None):
     pf = prefill_flops(PREFILL_B, PREFILL_S)
     db = decode_bytes(DECODE_B, DECODE_CTX)
     peaks = load_peaks()
@@ -507,8 +543,8 @@ def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_ma
         cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": nt, "kind": "oracle",
                "sample": f"{rows} random prefill query rows of the workload, {dt:.1f} s of oracle work on "
                          f"{os.cpu_count()} host cores"}
-    tr_pre = NCU_TRAFFIC_BYTES["prefill"]
-    tr_dec = NCU_TRAFFIC_BYTES["decode"]
+    tr_pre, tr_pre_src = traffic("prefill")
+    tr_dec, tr_dec_src = traffic("decode")
     line = {
         "metric": METRIC,
         "value": pre_tflops,
@@ -534,11 +570,11 @@ def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_ma
             "value": dec_gbs, "unit": "GB/s", "ms": dec_ms_max,
             "roofline": {"bound": "hbm", "achieved": dec_per_launch, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": dec_per_launch / peaks["hbm_gbs"],
-                         "traffic": tr_dec, "peak_source": peaks["source"]},
+                         "traffic": tr_dec, "traffic_source": tr_dec_src, "peak_source": peaks["source"]},
         },
         "roofline": {
             "bound": "tensor", "achieved": pre_per_launch, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": pre_per_launch / peaks["bf16_tflops"], "traffic": tr_pre,
+            "frac": pre_per_launch / peaks["bf16_tflops"], "traffic": tr_pre, "traffic_source": tr_pre_src,
             "kernel": "kb_prefill_kernel_s2", "peak_source": peaks["source"] + " burst bf16",
             "frac_of_sustained": pre_per_launch / peaks["bf16_tflops_sustained"],
         },
@@ -573,27 +609,29 @@ def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_ma
                          "kernel": "kb_bwd_delta_kernel + kb_bwd_dq_kernel + kb_bwd_dkdv_kernel (one call)",
                          "peak_source": peaks["source"] + " burst bf16"},
         }
+    if grid is not None:
+        line["grid"] = grid
     print(json.dumps(line), flush=True)
 
 
-def run_sweep(args, local):
-    """Time the pages' grid (prefill S x B, decode ctx x B), one JSON line per
-    configuration.  L2 is flushed before every timed launch by reading a 512 MB
-    buffer (a read, so no dirty lines are left for the kernel to write back)."""
+GRID_PREFILL_S = (1024, 4096, 8192, 16384)
+GRID_DECODE_CTX = (128, 1024, 4096, 8192)
+GRID_B = (1, 4, 8, 16)
+
+
+def time_grid(kb_attn, peaks, prefill_batches, reps, device):
+    """The configuration grid of the KernelBraid README ("Performance":
+    prefill at S in 1K..16K, decode at B in 1..16 x ctx in 128..8K), each
+    configuration timed alone with CUDA events, L2 flushed before every timed
+    launch by reading a 512 MB buffer (a read leaves no dirty lines for the
+    kernel to write back).  Returns one record per configuration."""
     import torch
 
-    from bitwise_aligned_causal_gb300 import build
+    flush = torch.ones(128 << 20, dtype=torch.float32, device=device)
+    sink = torch.empty(1, dtype=torch.float32, device=device)
+    gen = torch.Generator(device=device)
 
-    torch.cuda.set_device(local)
-    build.build()
-    from bitwise_aligned_causal_gb300 import kb_attn
-
-    peaks = load_peaks()
-    flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
-    sink = torch.empty(1, dtype=torch.float32, device="cuda")
-    gen = torch.Generator(device="cuda")
-
-    def timed(fn, reps):
+    def timed(fn):
         ts = []
         for i in range(reps + 3):
             torch.sum(flush, dim=0, keepdim=True, out=sink)
@@ -607,31 +645,65 @@ def run_sweep(args, local):
                 ts.append(a.elapsed_time(b))
         return statistics.median(ts)
 
-    for S in (1024, 4096, 8192, 16384):
-        for B in (1, 4, 8, 16):
+    out = []
+    for S in GRID_PREFILL_S:
+        for B in prefill_batches:
             gen.manual_seed(8_000_000 + 100 * (S // 1024) + B)
-            q = torch.randn(B, HQ, S, D, device="cuda", dtype=torch.bfloat16, generator=gen)
-            k = torch.randn(B, HKV, S, D, device="cuda", dtype=torch.bfloat16, generator=gen)
-            v = torch.randn(B, HKV, S, D, device="cuda", dtype=torch.bfloat16, generator=gen)
+            q = torch.randn(B, HQ, S, D, device=device, dtype=torch.bfloat16, generator=gen)
+            k = torch.randn(B, HKV, S, D, device=device, dtype=torch.bfloat16, generator=gen)
+            v = torch.randn(B, HKV, S, D, device=device, dtype=torch.bfloat16, generator=gen)
             o = torch.empty_like(q)
-            ms = timed(lambda: kb_attn.prefill(q, k, v, out=o), args.steps)
+            ms = timed(lambda: kb_attn.prefill(q, k, v, out=o))
             tf = prefill_flops(B, S) / (ms / 1e3) / 1e12
-            print(json.dumps({"kind": "prefill", "S": S, "B": B, "ms": ms, "TFLOP/s": tf,
-                              "frac": tf / peaks["bf16_tflops"], "peak_source": peaks["source"]}), flush=True)
+            out.append({"kind": "prefill", "S": S, "B": B, "ms": ms, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]})
             del q, k, v, o
-    for ctx in (128, 1024, 4096, 8192):
-        for B in (1, 4, 8, 16):
+    for ctx in GRID_DECODE_CTX:
+        for B in GRID_B:
             gen.manual_seed(9_000_000 + ctx + B)
-            q = torch.randn(B, HQ, 1, D, device="cuda", dtype=torch.bfloat16, generator=gen)
-            k = torch.randn(B, HKV, ctx, D, device="cuda", dtype=torch.bfloat16, generator=gen)
-            v = torch.randn(B, HKV, ctx, D, device="cuda", dtype=torch.bfloat16, generator=gen)
+            q = torch.randn(B, HQ, 1, D, device=device, dtype=torch.bfloat16, generator=gen)
+            k = torch.randn(B, HKV, ctx, D, device=device, dtype=torch.bfloat16, generator=gen)
+            v = torch.randn(B, HKV, ctx, D, device=device, dtype=torch.bfloat16, generator=gen)
             o = torch.empty_like(q)
-            ms = timed(lambda: kb_attn.decode(q, k, v, ctx, out=o), args.steps)
+            ms = timed(lambda: kb_attn.decode(q, k, v, ctx, out=o))
             gbs = decode_bytes(B, ctx) / (ms / 1e3) / 1e9
-            print(json.dumps({"kind": "decode", "ctx": ctx, "B": B, "us": ms * 1e3, "GB/s": gbs,
-                              "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}), flush=True)
+            out.append({"kind": "decode", "ctx": ctx, "B": B, "us": ms * 1e3, "GB/s": gbs,
+                        "frac": gbs / peaks["hbm_gbs"]})
             del q, k, v, o
     kb_attn.check_device_status()
+    return out
+
+
+def grid_summary(records, peaks):
+    """The grid as the KernelBraid README ("Performance") reports it: the prefill bar over S at B=1 and the
+    decode bar over all 16 (B, ctx) cells, here as mean fractions of roofline."""
+    pre = [r for r in records if r["kind"] == "prefill" and r["B"] == 1]
+    dec = [r for r in records if r["kind"] == "decode"]
+    return {
+        "workload": ("KernelBraid README grid: prefill B=1, S in 1K/4K/8K/16K; decode B in 1/4/8/16 x ctx in 128/1K/4K/8K; "
+                     "Hq=32 Hkv=8 D=128 bf16, torch.randn inputs; L2 flushed (512 MB read) before each timed "
+                     "launch; median of the timed launches"),
+        "prefill_b1": {str(r["S"]): {"TFLOP/s": round(r["TFLOP/s"], 1), "frac": round(r["frac"], 4)} for r in pre},
+        "decode": {f"B{r['B']}_ctx{r['ctx']}": {"GB/s": round(r["GB/s"], 1), "us": round(r["us"], 2),
+                                                "frac": round(r["frac"], 4)} for r in dec},
+        "prefill_bar_mean_frac": statistics.mean(r["frac"] for r in pre),
+        "decode_bar_mean_frac": statistics.mean(r["frac"] for r in dec),
+        "peaks": {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "source": peaks["source"]},
+    }
+
+
+def run_sweep(args, local):
+    """Time the whole grid (prefill S x B, decode ctx x B), one JSON line per configuration."""
+    import torch
+
+    from bitwise_aligned_causal_gb300 import build
+
+    torch.cuda.set_device(local)
+    build.build()
+    from bitwise_aligned_causal_gb300 import kb_attn
+
+    peaks = load_peaks()
+    for r in time_grid(kb_attn, peaks, GRID_B, args.steps, torch.device("cuda", local)):
+        print(json.dumps(dict(r, peak_source=peaks["source"])), flush=True)
 
 
 def main():
@@ -645,6 +717,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip timing the training forward + backward")
     ap.add_argument("--no-segmented", action="store_true", help="skip timing the small-batch segmented decode")
+    ap.add_argument("--no-grid", action="store_true", help="skip timing the README's configuration grid")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="full")
     ap.add_argument("--sweep", action="store_true",
                     help="time every prefill (S x B) and decode (ctx x B) configuration of the grid instead")

@@ -366,13 +366,15 @@ kb_status kb_attn_decode_seg(const void* q, const void* k, const void* v, void* 
 
 kb_status kb_attn_decode_seg_static(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv,
                                     int ctx_len, int kv_cap, int seg_tiles, void* stream) {
+  // the argument checks every entry point makes come first, so a bad
+  // pointer or head count gets the same status here as elsewhere
+  kb_status s = check_ptrs(q, k, v, o);
+  if (s != KB_OK) return s;
+  if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
   if (ctx_len < 1 || ctx_len > kv_cap || seg_tiles < 1) return KB_ERR_INVALID_ARG;
   const size_t need = kb_attn_seg_workspace_bytes(B, Hq, 1, ctx_len - 1, seg_tiles);
   if (need == 0) return KB_ERR_INVALID_ARG;
   if (need > kSegScratchFloats * sizeof(float)) return KB_ERR_UNSUPPORTED;
-  kb_status s = check_ptrs(q, k, v, o);
-  if (s != KB_OK) return s;
-  if ((s = check_heads(B, Hq, Hkv)) != KB_OK) return s;
   DeviceState* dst = nullptr;
   if ((s = get_device_state(&dst)) != KB_OK) return s;
   return chunk_impl(q, k, v, o, B, Hq, Hkv, 1, ctx_len - 1, kv_cap, 0, stream, nullptr, nullptr, nullptr, seg_tiles,

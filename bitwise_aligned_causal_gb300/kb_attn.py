@@ -14,6 +14,8 @@ from __future__ import annotations
 import ctypes
 import os
 
+from . import shapes
+
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkb_attn.so")
 
@@ -162,6 +164,17 @@ def kb_attn_debug_wait_timeout(limit_us, stream=None) -> int:
 
 
 # ------------------------------------------------------------------ torch marshalling
+#
+# Every wrapper below checks each tensor's dtype, layout, device and full
+# shape against the others (shapes.py) before the C call, so a caller's
+# mistake raises here instead of becoming an out-of-bounds device access.
+#
+# Outputs are complete once the stream has run the kernels.  A bounded
+# device-side wait that gave up, or a device-resident argument found out of
+# range (a page index, a per-sequence length), leaves the affected rows
+# unwritten and is reported only by check_device_status(), which also clears
+# the library's error word; until that word is cleared, later calls on the
+# device skip their work.  Pass check=True to call it after the launch.
 
 def _torch():
     import torch
@@ -175,7 +188,13 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _check(t, name, ndim):
+def _on_current_device(t, name):
+    torch = _torch()
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, not on the current device cuda:{torch.cuda.current_device()}")
+
+
+def _check(t, name, ndim=4):
     torch = _torch()
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
@@ -185,6 +204,21 @@ def _check(t, name, ndim):
         raise ValueError(f"{name} must be contiguous")
     if t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dimensions [batch, heads, seq, head_dim]")
+    _on_current_device(t, name)
+
+
+def _check_i32(t, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
+    _on_current_device(t, name)
+
+
+def _check_f32(t, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous float32 CUDA tensor")
+    _on_current_device(t, name)
 
 
 def _raise(status, where):
@@ -192,161 +226,170 @@ def _raise(status, where):
         raise KBError(status, where)
 
 
-def prefill(q, k, v, out=None, stream=None):
-    """Causal prefill: q [B,Hq,S,128], k/v [B,Hkv,S,128] -> o shaped like q."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, 4)
-    B, Hq, S, _ = q.shape
-    Hkv = k.shape[1]
+def _out(q, out):
     o = _torch().empty_like(q) if out is None else out
-    _check(o, "out", 4)
-    _raise(kb_attn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, S, _stream(stream)),
-           "kb_attn_prefill")
+    _check(o, "out")
     return o
 
 
-def chunk(q, k, v, start, out=None, stream=None, q_tiles_per_cta=None):
+def _finish(status, where, check, stream):
+    _raise(status, where)
+    if check:
+        check_device_status(stream)
+
+
+def prefill(q, k, v, out=None, stream=None, check=False):
+    """Causal prefill: q [B,Hq,S,128], k/v [B,Hkv,S,128] -> o shaped like q."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    if out is not None:
+        _check(out, "out")
+    B, Hq, Hkv, S = shapes.prefill(q.shape, k.shape, v.shape, None if out is None else out.shape)
+    o = _out(q, out)
+    _finish(kb_attn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, S, _stream(stream)),
+            "kb_attn_prefill", check, stream)
+    return o
+
+
+def chunk(q, k, v, start, out=None, stream=None, q_tiles_per_cta=None, check=False):
     """Chunked forward: q [B,Hq,L,128] at positions start.., k/v caches [B,Hkv,cap,128]."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, 4)
-    B, Hq, L, _ = q.shape
-    Hkv, cap = k.shape[1], k.shape[2]
-    o = _torch().empty_like(q) if out is None else out
-    _check(o, "out", 4)
+        _check(t, n)
+    if out is not None:
+        _check(out, "out")
+    B, Hq, Hkv, L, cap = shapes.chunk(q.shape, k.shape, v.shape, int(start), None if out is None else out.shape)
+    o = _out(q, out)
     if q_tiles_per_cta is None:
         st = kb_attn_chunk(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, L, int(start), cap,
                            _stream(stream))
     else:
         st = kb_attn_chunk_cta_shape(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, L,
                                      int(start), cap, int(q_tiles_per_cta), _stream(stream))
-    _raise(st, "kb_attn_chunk")
+    _finish(st, "kb_attn_chunk", check, stream)
     return o
 
 
-def decode(q, k, v, ctx_len, out=None, stream=None):
+def decode(q, k, v, ctx_len, out=None, stream=None, check=False):
     """One-token decode: q [B,Hq,1,128] at position ctx_len-1, k/v caches [B,Hkv,cap,128]."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, 4)
-    B, Hq = q.shape[0], q.shape[1]
-    Hkv, cap = k.shape[1], k.shape[2]
-    o = _torch().empty_like(q) if out is None else out
-    _check(o, "out", 4)
-    _raise(kb_attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, int(ctx_len), cap,
-                          _stream(stream)), "kb_attn_decode")
+        _check(t, n)
+    if out is not None:
+        _check(out, "out")
+    B, Hq, Hkv, cap = shapes.decode(q.shape, k.shape, v.shape, int(ctx_len), None if out is None else out.shape)
+    o = _out(q, out)
+    _finish(kb_attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, int(ctx_len), cap,
+                           _stream(stream)), "kb_attn_decode", check, stream)
     return o
 
 
-def decode_paged(q, k_pages, v_pages, block_table, ctx_lens, out=None, stream=None):
+def decode_paged(q, k_pages, v_pages, block_table, ctx_lens, out=None, stream=None, check=False):
     """Paged decode: q [B,Hq,1,128]; pools [num_pages,Hkv,page_size,128]; block_table int32 [B,pages_per_seq];
     ctx_lens int32 [B] (all on the device)."""
-    torch = _torch()
     for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages")):
-        _check(t, n, 4)
+        _check(t, n)
     for t, n in ((block_table, "block_table"), (ctx_lens, "ctx_lens")):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
-            raise TypeError(f"{n} must be a contiguous int32 CUDA tensor")
-    B, Hq = q.shape[0], q.shape[1]
-    num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
-    o = torch.empty_like(q) if out is None else out
-    _check(o, "out", 4)
-    _raise(kb_attn_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), o.data_ptr(), B, Hq, Hkv,
-                                block_table.data_ptr(), block_table.shape[1], page_size, num_pages,
-                                ctx_lens.data_ptr(), _stream(stream)), "kb_attn_decode_paged")
+        _check_i32(t, n)
+    if out is not None:
+        _check(out, "out")
+    B, Hq, Hkv, num_pages, page_size, pps = shapes.decode_paged(
+        q.shape, k_pages.shape, v_pages.shape, block_table.shape, ctx_lens.shape, None if out is None else out.shape)
+    o = _out(q, out)
+    _finish(kb_attn_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), o.data_ptr(), B, Hq, Hkv,
+                                 block_table.data_ptr(), pps, page_size, num_pages, ctx_lens.data_ptr(),
+                                 _stream(stream)), "kb_attn_decode_paged", check, stream)
     return o
 
 
-def chunk_paged(q, k_pages, v_pages, block_table, start, out=None, stream=None):
+def chunk_paged(q, k_pages, v_pages, block_table, start, out=None, stream=None, check=False):
     """Chunked forward over a paged cache: q [B,Hq,L,128] at positions start..; pools
     [num_pages,Hkv,page_size,128]; block_table int32 [B,pages_per_seq] on the device."""
-    torch = _torch()
     for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages")):
-        _check(t, n, 4)
-    if not isinstance(block_table, torch.Tensor) or not block_table.is_cuda or block_table.dtype != torch.int32:
-        raise TypeError("block_table must be an int32 CUDA tensor")
-    B, Hq, L = q.shape[0], q.shape[1], q.shape[2]
-    num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
-    o = torch.empty_like(q) if out is None else out
-    _check(o, "out", 4)
-    _raise(kb_attn_chunk_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), o.data_ptr(), B, Hq, Hkv, L,
-                               int(start), block_table.data_ptr(), block_table.shape[1], page_size, num_pages,
-                               _stream(stream)), "kb_attn_chunk_paged")
+        _check(t, n)
+    _check_i32(block_table, "block_table")
+    if out is not None:
+        _check(out, "out")
+    B, Hq, Hkv, L, num_pages, page_size, pps = shapes.chunk_paged(
+        q.shape, k_pages.shape, v_pages.shape, block_table.shape, int(start), None if out is None else out.shape)
+    o = _out(q, out)
+    _finish(kb_attn_chunk_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), o.data_ptr(), B, Hq, Hkv, L,
+                                int(start), block_table.data_ptr(), pps, page_size, num_pages, _stream(stream)),
+            "kb_attn_chunk_paged", check, stream)
     return o
 
 
-def chunk_varlen(q, k, v, starts, lens, out=None, block_table=None, stream=None):
+def chunk_varlen(q, k, v, starts, lens, out=None, block_table=None, stream=None, check=False):
     """Ragged batch: q [B,Hq,L_max,128]; per-sequence starts/lens int32 [B] on the device; k/v either
     contiguous caches [B,Hkv,cap,128] or, with block_table [B,pages_per_seq], pools [num_pages,Hkv,page,128]."""
-    torch = _torch()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, 4)
+        _check(t, n)
     for t, n in ((starts, "starts"), (lens, "lens")) + (((block_table, "block_table"),) if block_table is not None
                                                          else ()):
-        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
-            raise TypeError(f"{n} must be a contiguous int32 CUDA tensor")
-    B, Hq, L_max = q.shape[0], q.shape[1], q.shape[2]
-    o = torch.empty_like(q) if out is None else out
-    _check(o, "out", 4)
+        _check_i32(t, n)
+    if out is not None:
+        _check(out, "out")
+    sz = shapes.varlen(q.shape, k.shape, v.shape, starts.shape, lens.shape,
+                       None if block_table is None else block_table.shape, None if out is None else out.shape)
+    o = _out(q, out)
     if block_table is None:
-        Hkv, cap = k.shape[1], k.shape[2]
+        B, Hq, Hkv, L_max, cap = sz
         st = kb_attn_chunk_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, L_max,
                                   starts.data_ptr(), lens.data_ptr(), cap, None, 0, 0, 0, _stream(stream))
     else:
-        num_pages, Hkv, page_size = k.shape[0], k.shape[1], k.shape[2]
+        B, Hq, Hkv, L_max, num_pages, page_size, pps = sz
         st = kb_attn_chunk_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, L_max,
-                                  starts.data_ptr(), lens.data_ptr(), 0, block_table.data_ptr(),
-                                  block_table.shape[1], page_size, num_pages, _stream(stream))
-    _raise(st, "kb_attn_chunk_varlen")
+                                  starts.data_ptr(), lens.data_ptr(), 0, block_table.data_ptr(), pps, page_size,
+                                  num_pages, _stream(stream))
+    _finish(st, "kb_attn_chunk_varlen", check, stream)
     return o
 
 
 def check_device_status(stream=None):
+    """Wait for `stream`, then raise KBError if a kernel since the last check gave up on a wait
+    (KB_ERR_TIMEOUT) or found a device-resident argument out of range (KB_ERR_INVALID_ARG)."""
     _raise(kb_attn_check_device_status(_stream(stream)), "kb_attn_check_device_status")
 
 
-def _check_f32(t, name, shape):
-    torch = _torch()
-    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
-        raise TypeError(f"{name} must be a contiguous float32 CUDA tensor")
-    if tuple(t.shape) != tuple(shape):
-        raise ValueError(f"{name} must have shape {tuple(shape)}")
-
-
-def prefill_lse(q, k, v, out=None, lse=None, stream=None):
+def prefill_lse(q, k, v, out=None, lse=None, stream=None, check=False):
     """Training forward: (o, lse) with o bit-identical to prefill and lse [B,Hq,S] float32 the
     natural-log log-sum-exp of each row's scaled scores."""
     torch = _torch()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, 4)
-    B, Hq, S, _ = q.shape
-    Hkv = k.shape[1]
-    o = torch.empty_like(q) if out is None else out
-    _check(o, "out", 4)
+        _check(t, n)
+    if out is not None:
+        _check(out, "out")
+    B, Hq, Hkv, S = shapes.prefill(q.shape, k.shape, v.shape, None if out is None else out.shape)
+    o = _out(q, out)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check_f32(lse, "lse", (B, Hq, S))
-    _raise(kb_attn_prefill_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv,
-                               S, _stream(stream)), "kb_attn_prefill_lse")
+    _check_f32(lse, "lse")
+    shapes.vector_f32("lse", lse.shape, B, Hq, S)
+    _finish(kb_attn_prefill_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv,
+                                S, _stream(stream)), "kb_attn_prefill_lse", check, stream)
     return o, lse
 
 
-def backward(q, k, v, o, dout, lse, delta=None, dq=None, dk=None, dv=None, stream=None):
+def backward(q, k, v, o, dout, lse, delta=None, dq=None, dk=None, dv=None, stream=None, check=False):
     """Gradients (dq, dk, dv) of the whole-sequence causal prefill for output gradient dout; o and
     lse from prefill_lse.  Also returns delta [B,Hq,S] float32 = rowsum(dout * o)."""
     torch = _torch()
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
-        _check(t, n, 4)
-    B, Hq, S, _ = q.shape
-    Hkv = k.shape[1]
-    _check_f32(lse, "lse", (B, Hq, S))
+        _check(t, n)
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        if t is not None:
+            _check(t, n)
+    B, Hq, Hkv, S = shapes.backward(q.shape, k.shape, v.shape, o.shape, dout.shape,
+                                    None if dq is None else dq.shape, None if dk is None else dk.shape,
+                                    None if dv is None else dv.shape)
+    _check_f32(lse, "lse")
+    shapes.vector_f32("lse", lse.shape, B, Hq, S)
     delta = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if delta is None else delta
-    _check_f32(delta, "delta", (B, Hq, S))
+    _check_f32(delta, "delta")
+    shapes.vector_f32("delta", delta.shape, B, Hq, S)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
-        _check(t, n, 4)
-    _raise(kb_attn_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
-                            delta.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, S,
-                            _stream(stream)), "kb_attn_backward")
+    _finish(kb_attn_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                             delta.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, S,
+                             _stream(stream)), "kb_attn_backward", check, stream)
     return dq, dk, dv, delta
 
 
@@ -356,57 +399,63 @@ def _workspace(nbytes, device, workspace):
         return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
     if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or not workspace.is_contiguous():
         raise TypeError("workspace must be a contiguous CUDA tensor")
+    _on_current_device(workspace, "workspace")
     return workspace
 
 
-def prefill_seg(q, k, v, seg_tiles, out=None, stream=None):
+def prefill_seg(q, k, v, seg_tiles, out=None, stream=None, check=False):
     """Segmented-mode prefill (segments of seg_tiles 128-key tiles, folded left to right)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, 4)
-    B, Hq, S, _ = q.shape
-    o = _torch().empty_like(q) if out is None else out
-    _check(o, "out", 4)
-    _raise(kb_attn_prefill_seg(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, k.shape[1], S,
-                               int(seg_tiles), _stream(stream)), "kb_attn_prefill_seg")
+        _check(t, n)
+    if out is not None:
+        _check(out, "out")
+    B, Hq, Hkv, S = shapes.prefill(q.shape, k.shape, v.shape, None if out is None else out.shape)
+    o = _out(q, out)
+    _finish(kb_attn_prefill_seg(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, S,
+                                int(seg_tiles), _stream(stream)), "kb_attn_prefill_seg", check, stream)
     return o
 
 
-def chunk_seg(q, k, v, start, seg_tiles, out=None, workspace=None, stream=None):
+def chunk_seg(q, k, v, start, seg_tiles, out=None, workspace=None, stream=None, check=False):
     """Segmented-mode chunk: q [B,Hq,L,128] at positions start.., caches [B,Hkv,cap,128]."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, 4)
-    B, Hq, L, _ = q.shape
-    o = _torch().empty_like(q) if out is None else out
-    _check(o, "out", 4)
+        _check(t, n)
+    if out is not None:
+        _check(out, "out")
+    B, Hq, Hkv, L, cap = shapes.chunk(q.shape, k.shape, v.shape, int(start), None if out is None else out.shape)
+    o = _out(q, out)
     ws = _workspace(kb_attn_seg_workspace_bytes(B, Hq, L, int(start), int(seg_tiles)), q.device, workspace)
-    _raise(kb_attn_chunk_seg(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, k.shape[1], L,
-                             int(start), k.shape[2], int(seg_tiles), ws.data_ptr(), ws.numel() * ws.element_size(),
-                             _stream(stream)), "kb_attn_chunk_seg")
+    _finish(kb_attn_chunk_seg(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, L, int(start), cap,
+                              int(seg_tiles), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+            "kb_attn_chunk_seg", check, stream)
     return o
 
 
-def decode_seg(q, k, v, ctx_len, seg_tiles, out=None, workspace=None, stream=None):
+def decode_seg(q, k, v, ctx_len, seg_tiles, out=None, workspace=None, stream=None, check=False):
     """Segmented-mode decode: q [B,Hq,1,128] at position ctx_len-1."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, 4)
-    B, Hq = q.shape[0], q.shape[1]
-    o = _torch().empty_like(q) if out is None else out
-    _check(o, "out", 4)
+        _check(t, n)
+    if out is not None:
+        _check(out, "out")
+    B, Hq, Hkv, cap = shapes.decode(q.shape, k.shape, v.shape, int(ctx_len), None if out is None else out.shape)
+    o = _out(q, out)
     ws = _workspace(kb_attn_seg_workspace_bytes(B, Hq, 1, int(ctx_len) - 1, int(seg_tiles)), q.device, workspace)
-    _raise(kb_attn_decode_seg(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, k.shape[1],
-                              int(ctx_len), k.shape[2], int(seg_tiles), ws.data_ptr(),
-                              ws.numel() * ws.element_size(), _stream(stream)), "kb_attn_decode_seg")
+    _finish(kb_attn_decode_seg(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, int(ctx_len), cap,
+                               int(seg_tiles), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+            "kb_attn_decode_seg", check, stream)
     return o
 
 
-def decode_seg_static(q, k, v, ctx_len, seg_tiles, out=None, stream=None):
-    """Segmented-mode decode with the library's own scratch (no workspace argument, no allocation)."""
+def decode_seg_static(q, k, v, ctx_len, seg_tiles, out=None, stream=None, check=False):
+    """Segmented-mode decode with the library's own scratch (no workspace argument, no allocation).
+    Calls that overlap on the GPU share that scratch and must not run at the same time."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, 4)
-    B, Hq = q.shape[0], q.shape[1]
-    o = _torch().empty_like(q) if out is None else out
-    _check(o, "out", 4)
-    _raise(kb_attn_decode_seg_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, k.shape[1],
-                                     int(ctx_len), k.shape[2], int(seg_tiles), _stream(stream)),
-           "kb_attn_decode_seg_static")
+        _check(t, n)
+    if out is not None:
+        _check(out, "out")
+    B, Hq, Hkv, cap = shapes.decode(q.shape, k.shape, v.shape, int(ctx_len), None if out is None else out.shape)
+    o = _out(q, out)
+    _finish(kb_attn_decode_seg_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv,
+                                      int(ctx_len), cap, int(seg_tiles), _stream(stream)),
+            "kb_attn_decode_seg_static", check, stream)
     return o

@@ -26,6 +26,17 @@
  *    default stream) and do not synchronise the host.  Argument errors are
  *    reported before anything is enqueued.  A device-side wait that gave up
  *    (never expected) is reported by kb_attn_check_device_status.
+ *  - Outputs are valid only once kb_attn_check_device_status has returned
+ *    KB_OK after the call.  KB_OK from an entry point means only that the
+ *    arguments passed the host checks and the kernels were enqueued.  When a
+ *    kernel gives up on a wait or finds a device-resident argument out of
+ *    range (a page index, a per-sequence length) it records that in the
+ *    library's per-device error word; until kb_attn_check_device_status reads
+ *    and clears that word, every later kernel on the device skips its work
+ *    and leaves its output unwritten, although its entry point returns KB_OK.
+ *  - The sizes are all the library sees of the buffers: it cannot check that
+ *    a buffer is as large as its shape says.  A caller that passes sizes
+ *    larger than its allocations makes the kernels read or write past them.
  *  - Rows of the KV cache beyond the visible context are never used, so they
  *    may hold anything (including NaN bit patterns).
  */
@@ -192,10 +203,18 @@ kb_status kb_attn_decode_seg(const void* q, const void* k, const void* v, void* 
  * kb_attn_decode_seg without a caller workspace: the partials go to a 4 MiB
  * scratch array the library owns (one per device, part of the loaded module),
  * so the call allocates nothing and takes nothing but the decode's tensors.
+ * It serves callers that cannot allocate device memory at the point of the
+ * call: a serving loop whose memory pool is already handed out, or code that
+ * must not enter the CUDA allocator (which may synchronise the device) in its
+ * decode step.  No paper counterpart: it is a deployment variant of
+ * kb_attn_decode_seg.
  * Requests needing more than 4 MiB of partials (B * Hq * segments * 528 bytes)
- * return KB_ERR_UNSUPPORTED.  The scratch is shared: calls of this entry point
- * on one device must not overlap (issue them on one stream).  Bits equal
- * kb_attn_decode_seg's.
+ * return KB_ERR_UNSUPPORTED before anything is enqueued.  The scratch is
+ * shared and keeps the last call's contents (every call overwrites the part
+ * it reads): calls of this entry point on one device that overlap on the GPU
+ * race, so issue them on one stream.  The first call of any entry point on a
+ * device looks up the scratch's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture.  Bits equal kb_attn_decode_seg's.
  */
 kb_status kb_attn_decode_seg_static(const void* q, const void* k, const void* v, void* o,
                                     int B, int Hq, int Hkv, int ctx_len, int kv_cap, int seg_tiles,

@@ -84,3 +84,25 @@ def test_reference_arm_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_grid_summary_reports_both_bars():
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 8000.0, "source": "measured"}
+    recs = [{"kind": "prefill", "S": S, "B": 1, "ms": 1.0, "TFLOP/s": 1000.0, "frac": 0.5}
+            for S in bench.GRID_PREFILL_S]
+    recs += [{"kind": "decode", "ctx": c, "B": b, "us": 10.0, "GB/s": 4000.0, "frac": 0.5}
+             for c in bench.GRID_DECODE_CTX for b in bench.GRID_B]
+    g = bench.grid_summary(recs, peaks)
+    assert len(g["prefill_b1"]) == 4 and len(g["decode"]) == 16
+    assert g["prefill_bar_mean_frac"] == pytest.approx(0.5) and g["decode_bar_mean_frac"] == pytest.approx(0.5)
+    d = _emit(grid=g)
+    assert d["grid"]["decode"]["B1_ctx8192"]["frac"] == 0.5
+
+
+def test_traffic_is_null_unless_captured_on_the_current_sources():
+    b, src = bench.traffic("prefill")
+    assert src["current_sources"] == bench.sources_hash("prefill")
+    if src["captured_on_sources"] != src["current_sources"]:
+        assert b is None and src["fresh"] is False
+    else:
+        assert b is not None and src["fresh"] is True

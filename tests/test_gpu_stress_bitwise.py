@@ -1,0 +1,201 @@
+"""Every entry point, bit for bit, on inputs that make the rescale branch fire.
+
+The contract's row function rescales a row's O only when its reference max
+moves after the first key tile (a later tile's max more than 64 raw score
+units above it).  On iid N(0, 1) inputs that never happens, so the bitwise
+tests on such inputs cover only the no-rescale path.  Here every entry point
+runs on the stress recipe (q, k ~ N(0, 8^2), 1% of key rows x32, v ~ N(0, 1);
+the peaked-softmax workload of the pages' grid), and the host first checks,
+by replaying the decision with an fp32 error margin, that most of the rows
+compared really move their max after tile 0.
+
+Compared with the stress prefill, bit for bit (KernelBraid README,
+"Advantages": bitwise-identical prefill and incremental decode across the
+supported workloads):
+  - a seeded random partition into chunks of 1-2 rows (packed kernel, narrow),
+    3-32 rows (packed kernel, wide) and 33-400 rows (tile kernel, start != 0);
+  - decodes at positions around key-tile boundaries;
+  - paged chunks, paged decode and a ragged batch;
+  - the tile kernel's CTA shapes 1-4 and the packed kernel;
+  - the segmented mode: prefill_seg = chunk_seg = decode_seg.
+Sampled rows of the default and the segmented prefill are checked against
+the fp64 oracle.
+"""
+
+import numpy as np
+import pytest
+
+from bitwise_aligned_causal_gb300 import inputs
+from tests.gpu_util import assert_close_to_oracle, from_dev, gather_rows, rescale_fraction, to_dev
+
+pytestmark = pytest.mark.gpu
+
+B, S, HQ, HKV, D = 2, 3000, 32, 8, 128
+SEED = 5_100_000
+
+
+@pytest.fixture(scope="module")
+def kb():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bitwise_aligned_causal_gb300 import build
+
+    build.build()
+    from bitwise_aligned_causal_gb300 import kb_attn
+
+    yield kb_attn
+    assert kb_attn.kb_attn_check_device_status(None) == kb_attn.KB_OK
+
+
+@pytest.fixture(scope="module")
+def stress(kb):
+    x = inputs.make_stress_qkv(B, S, SEED)
+    q, k, v = to_dev(x.q), to_dev(x.k), to_dev(x.v)
+    pre = kb.prefill(q, k, v)
+    kb.check_device_status()
+    return x, q, k, v, pre
+
+
+def _rows_at(positions):
+    return np.array([(b, h, p) for b in range(B) for h in range(HQ) for p in positions], dtype=np.int32)
+
+
+def _partition(rng, total):
+    """Chunks of 1-2, 3-32 and 33-400 rows in seeded random order."""
+    cuts, pos = [], 0
+    while pos < total:
+        kind = int(rng.integers(0, 3))
+        n = int(rng.integers(1, 3)) if kind == 0 else int(rng.integers(3, 33)) if kind == 1 else int(
+            rng.integers(33, 401))
+        n = min(n, total - pos)
+        cuts.append((pos, n))
+        pos += n
+    return cuts
+
+
+DECODE_POSITIONS = [0, 1, 126, 127, 128, 129, 255, 256, 257, 639, 640, 1023, 1024, 1025, 2047, 2048, 2559, 2999]
+
+
+def test_the_compared_rows_take_the_rescale_branch(stress):
+    """Host replay: most rows compared below move their reference max after key tile 0."""
+    x = stress[0]
+    rows = _rows_at([p for p in DECODE_POSITIONS if p >= 128])
+    assert rescale_fraction(x, rows) > 0.5
+    sampled = inputs.sample_rows(B, HQ, S, 16, seed=SEED + 1)
+    assert rescale_fraction(x, sampled[sampled[:, 2] >= 128]) > 0.5
+
+
+def test_prefill_against_the_oracle(kb, oracle_mod, stress):
+    x, _, _, _, pre = stress
+    rows = inputs.sample_rows(B, HQ, S, 8, seed=SEED + 2)
+    want = oracle_mod.attention_rows(x.q, x.k, x.v, rows)
+    assert_close_to_oracle(gather_rows(from_dev(pre), rows), want, "stress prefill")
+
+
+def test_random_partition_packed_and_tile_chunks(kb, stress):
+    import torch
+
+    _, q, k, v, pre = stress
+    rng = np.random.default_rng(SEED + 3)
+    cuts = _partition(rng, S)
+    sizes = [n for _, n in cuts]
+    assert min(sizes) <= 2 and any(3 <= n <= 32 for n in sizes) and max(sizes) > 32
+    assert any(n > 32 and s > 0 for s, n in cuts)
+    kc = torch.full_like(k, float("nan"))
+    vc = torch.full_like(v, float("nan"))
+    out = torch.empty_like(q)
+    for start, n in cuts:
+        kc[:, :, start:start + n] = k[:, :, start:start + n]
+        vc[:, :, start:start + n] = v[:, :, start:start + n]
+        out[:, :, start:start + n] = kb.chunk(q[:, :, start:start + n].contiguous(), kc, vc, start)
+    kb.check_device_status()
+    assert torch.equal(out.view(torch.int16), pre.view(torch.int16))
+
+
+def test_decodes_around_tile_boundaries(kb, stress):
+    import torch
+
+    _, q, k, v, pre = stress
+    for pos in DECODE_POSITIONS:
+        d = kb.decode(q[:, :, pos:pos + 1].contiguous(), k, v, pos + 1)
+        assert torch.equal(d[:, :, 0].view(torch.int16), pre[:, :, pos].view(torch.int16)), pos
+    kb.check_device_status()
+
+
+def test_cta_shapes_and_packed_kernel(kb, stress):
+    import torch
+
+    _, q, k, v, pre = stress
+    for shape in (1, 2, 3, 4):
+        o = kb.chunk(q, k, v, 0, q_tiles_per_cta=shape)
+        assert torch.equal(o.view(torch.int16), pre.view(torch.int16)), f"CTA shape {shape}"
+    for start, n in ((0, 32), (130, 20), (1000, 2), (2047, 3), (2968, 32)):
+        qc = q[:, :, start:start + n].contiguous()
+        for shape in (0, 1, 3, 4):
+            o = kb.chunk(qc, k, v, start, q_tiles_per_cta=shape)
+            assert torch.equal(o.view(torch.int16), pre[:, :, start:start + n].view(torch.int16)), (start, n, shape)
+    kb.check_device_status()
+
+
+def test_paged_and_ragged(kb, stress):
+    import torch
+
+    from tests.test_gpu_packed_paged import _paged
+
+    _, q, k, v, pre = stress
+    # paged decode, one context per sequence
+    ctx = np.array([2999 + 1, 1025], dtype=np.int32)
+    for page in (128, 256):
+        kp, vp, table = _paged(k, v, ctx, page, seed=SEED + page)
+        qd = torch.stack([q[b, :, int(c) - 1] for b, c in enumerate(ctx)])[:, :, None, :].contiguous()
+        dp = kb.decode_paged(qd, kp, vp, table, torch.tensor(ctx, device="cuda"))
+        for b, c in enumerate(ctx):
+            assert torch.equal(dp[b, :, 0].view(torch.int16), pre[b, :, int(c) - 1].view(torch.int16)), (page, b)
+    # paged chunks: a tile-kernel chunk and a packed chunk
+    for start, n in ((700, 900), (2100, 17)):
+        filled = np.full(B, start + n, dtype=np.int32)
+        kp, vp, table = _paged(k, v, filled, 256, seed=SEED + start)
+        o = kb.chunk_paged(q[:, :, start:start + n].contiguous(), kp, vp, table, start)
+        assert torch.equal(o.view(torch.int16), pre[:, :, start:start + n].view(torch.int16)), (start, n)
+    # ragged batch: each sequence its own window
+    starts, lens = [129, 2000], [700, 31]
+    L_max = max(lens)
+    qr = torch.full((B, HQ, L_max, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    for b in range(B):
+        qr[b, :, :lens[b]] = q[b, :, starts[b]:starts[b] + lens[b]]
+    rag = kb.chunk_varlen(qr, k, v, torch.tensor(starts, dtype=torch.int32, device="cuda"),
+                          torch.tensor(lens, dtype=torch.int32, device="cuda"))
+    for b in range(B):
+        assert torch.equal(rag[b, :, :lens[b]].view(torch.int16),
+                           pre[b, :, starts[b]:starts[b] + lens[b]].view(torch.int16)), b
+    kb.check_device_status()
+
+
+@pytest.mark.parametrize("seg", [2, 5])
+def test_segmented_mode(kb, oracle_mod, stress, seg):
+    import torch
+
+    x, q, k, v, _ = stress
+    ps = kb.prefill_seg(q, k, v, seg)
+    kb.check_device_status()
+    rows = inputs.sample_rows(B, HQ, S, 6, seed=SEED + 10 + seg)
+    want = oracle_mod.attention_rows(x.q, x.k, x.v, rows)
+    assert_close_to_oracle(gather_rows(from_dev(ps), rows), want, f"stress prefill_seg seg={seg}")
+    # chunk_seg over a random partition (packed and tile chunks)
+    rng = np.random.default_rng(SEED + 20 + seg)
+    kc = torch.full_like(k, float("nan"))
+    vc = torch.full_like(v, float("nan"))
+    out = torch.empty_like(q)
+    for start, n in _partition(rng, S):
+        kc[:, :, start:start + n] = k[:, :, start:start + n]
+        vc[:, :, start:start + n] = v[:, :, start:start + n]
+        out[:, :, start:start + n] = kb.chunk_seg(q[:, :, start:start + n].contiguous(), kc, vc, start, seg)
+    assert torch.equal(out.view(torch.int16), ps.view(torch.int16))
+    # decode_seg around segment and tile boundaries
+    edges = [seg * 128 * m + d for m in range(1, 12) for d in (-1, 0, 1)]
+    for pos in sorted({p for p in edges + [0, 2999] if 0 <= p < S}):
+        d = kb.decode_seg(q[:, :, pos:pos + 1].contiguous(), k, v, pos + 1, seg)
+        assert torch.equal(d[:, :, 0].view(torch.int16), ps[:, :, pos].view(torch.int16)), pos
+    kb.check_device_status()

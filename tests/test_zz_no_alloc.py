@@ -73,3 +73,33 @@ def test_too_large_is_refused(kb):
     with pytest.raises(kb.KBError) as e:
         kb.decode_seg_static(q, k, k, ctx, 1)
     assert e.value.status == kb.KB_ERR_UNSUPPORTED
+
+
+def test_just_under_the_limit(kb):
+    """31 x 32 rows x 8 segments x 528 bytes = 4,190,208 bytes of partials, just
+    under the 4 MiB scratch: bits equal the caller-workspace call, and the
+    device status stays clean (nothing was written past the scratch)."""
+    B, ctx, seg = 31, 1024, 1
+    assert kb.kb_attn_seg_workspace_bytes(B, 32, 1, ctx - 1, seg) == 4_190_208 <= 4 << 20
+    x = inputs.make_qkv(B, ctx, seed=97_200)
+    q, k, v = to_dev(x.q), to_dev(x.k), to_dev(x.v)
+    qd = q[:, :, ctx - 1:].contiguous()
+    for _ in range(2):
+        a = from_dev(kb.decode_seg(qd, k, v, ctx, seg))
+        b = from_dev(kb.decode_seg_static(qd, k, v, ctx, seg))
+        assert kb.kb_attn_check_device_status(None) == kb.KB_OK
+        assert np.array_equal(a, b)
+
+
+def test_one_segment_over_the_limit_is_refused(kb):
+    import torch
+
+    # ctx 1025 needs a ninth segment: 31 x 32 x 9 x 528 = 4,713,984 bytes > 4 MiB
+    B, ctx = 31, 1025
+    assert kb.kb_attn_seg_workspace_bytes(B, 32, 1, ctx - 1, 1) > 4 << 20
+    q = torch.zeros((B, 32, 1, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((B, 8, ctx, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(kb.KBError) as e:
+        kb.decode_seg_static(q, k, k, ctx, 1)
+    assert e.value.status == kb.KB_ERR_UNSUPPORTED
+    assert kb.kb_attn_check_device_status(None) == kb.KB_OK
