@@ -48,8 +48,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the sources differ from that hash, the figure no longer describes the timed
 # build and the bench line reports traffic as null.
 NCU_TRAFFIC = {
-    "prefill": {"bytes": None, "sources": None, "profile": "profiles/launch_list_bench_full.md"},
-    "decode": {"bytes": None, "sources": None, "profile": "profiles/launch_list_bench_full.md"},
+    "prefill": {"bytes": 805.67e6 + 504.21e6, "sources": "668249ed6242cbc1",
+                "profile": "profiles/launch_list_bench_full.md"},
+    "decode": {"bytes": 537.09e6 + 0.31e6, "sources": "7b24ac5fd7482677",
+               "profile": "profiles/launch_list_bench_full.md"},
 }
 KERNEL_SOURCES = {
     "prefill": ["kb_prefill2.cu", "kb_contract.cuh", "kb_ptx.cuh", "kb_launch.h", "kb_host.cu"],
@@ -334,62 +336,14 @@ def run_ours(args, rank, world, local):
     else:
         e2e = run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_attn)
     bwd = None if args.no_backward else run_backward(args, q, k, v, stream, world, local, rank, kb_attn)
-    seg = None if args.no_segmented else run_segmented(args, stream, world, local, rank, kb_attn)
     grid = None
     if not args.no_grid:
         barrier(world, local)
-        grid = grid_summary(time_grid(kb_attn, load_peaks(), (1,), 5, dev), load_peaks())
+        grid = grid_summary(time_grid(kb_attn, load_peaks(), (1,), dev), load_peaks())
     if rank != 0:
         return
     emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks, x,
-              bwd, seg, grid)
-
-
-SEG_DECODE_B, SEG_DECODE_CTX, SEG_TILES = 1, 8192, 4
-
-
-def run_segmented(args, stream, world, local, rank, kb_attn):
-    """Small-batch decode (B=1, ctx 8192) in the default mode and in the
-    segmented mode (segments of SEG_TILES key tiles, one CTA each), each timed
-    alone; the decode's K/V (33.6 MB) fits in L2, so a 512 MB read flushes it
-    before every timed launch."""
-    import numpy as np
-    import torch
-
-    from bitwise_aligned_causal_gb300 import inputs
-
-    y = inputs.make_qkv(SEG_DECODE_B, SEG_DECODE_CTX, SEED_DECODE + 7 + 1000 * rank, Lq=1)
-
-    def to_dev(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(stream.device)
-
-    q, k, v = to_dev(y.q), to_dev(y.k), to_dev(y.v)
-    o = torch.empty_like(q)
-    ws = torch.empty(kb_attn.kb_attn_seg_workspace_bytes(SEG_DECODE_B, HQ, 1, SEG_DECODE_CTX - 1, SEG_TILES),
-                     dtype=torch.uint8, device=q.device)
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=q.device)
-    reps = max(5, min(args.steps, 20))
-
-    def timed(fn):
-        for _ in range(3):
-            fn()
-        total = 0.0
-        for _ in range(reps):
-            flush.sum()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            total += e0.elapsed_time(e1)
-        return total / reps
-
-    barrier(world, local)
-    d_ms = timed(lambda: kb_attn.decode(q, k, v, SEG_DECODE_CTX, out=o))
-    s_ms = timed(lambda: kb_attn.decode_seg(q, k, v, SEG_DECODE_CTX, SEG_TILES, out=o, workspace=ws))
-    kb_attn.check_device_status()
-    dev = "cuda" if world > 1 else "cpu"
-    return {"default_ms": reduce_max(d_ms, world, dev), "seg_ms": reduce_max(s_ms, world, dev), "reps": reps}
+              bwd, grid)
 
 
 def run_backward(args, q, k, v, stream, world, local, rank, kb_attn):
@@ -531,7 +485,7 @@ def run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_att
 
 
 def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_max, pre_tflops, dec_gbs, e2e, clocks,
-              x, bwd=None, seg=None, grid=None):
+              x, bwd=None, grid=None):
     pf = prefill_flops(PREFILL_B, PREFILL_S)
     db = decode_bytes(DECODE_B, DECODE_CTX)
     peaks = load_peaks()
@@ -583,17 +537,6 @@ def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_ma
         "gpu_launches": 2 * n,
         "clocks": clocks,
     }
-    if seg is not None:
-        sb = decode_bytes(SEG_DECODE_B, SEG_DECODE_CTX)
-        line["decode_small_batch"] = {
-            "workload": f"one-token decode B={SEG_DECODE_B} ctx={SEG_DECODE_CTX}, L2 flushed before each launch",
-            "default": {"value": aggregate(sb, world, seg["default_ms"] / 1e3) / 1e9, "unit": "GB/s",
-                        "us": seg["default_ms"] * 1e3},
-            "segmented": {"value": aggregate(sb, world, seg["seg_ms"] / 1e3) / 1e9, "unit": "GB/s",
-                          "us": seg["seg_ms"] * 1e3, "seg_tiles": SEG_TILES,
-                          "note": "contract C5: kb_attn_decode_seg, one CTA per (segment, b, kv head) + fold"},
-            "reps": seg["reps"],
-        }
     if bwd is not None:
         bf = 2.5 * pf                                   # dq, dk, dv: five products of the forward's size
         per_launch = bf / (bwd["bwd_ms_local"] / 1e3) / 1e12
@@ -619,56 +562,96 @@ GRID_DECODE_CTX = (128, 1024, 4096, 8192)
 GRID_B = (1, 4, 8, 16)
 
 
-def time_grid(kb_attn, peaks, prefill_batches, reps, device):
-    """The configuration grid of the KernelBraid README ("Performance":
-    prefill at S in 1K..16K, decode at B in 1..16 x ctx in 128..8K), each
-    configuration timed alone with CUDA events, L2 flushed before every timed
-    launch by reading a 512 MB buffer (a read leaves no dirty lines for the
-    kernel to write back).  Returns one record per configuration."""
+L2_BYTES = 129e6      # GB300 L2
+
+
+def rotating_launch_ms(make, launch, bytes_per_copy, device, min_launches=48):
+    """Mean device time (ms) of one launch, timed over back-to-back launches on
+    rotating copies of the inputs that together exceed L2 twice over (so no
+    launch finds its inputs in L2 and no flush kernel runs between launches).
+    The launches are captured in a CUDA graph when the stream allows it, so
+    host-side launch cost does not enter; otherwise they are enqueued
+    directly.  Returns (ms, copies, method)."""
     import torch
 
-    flush = torch.ones(128 << 20, dtype=torch.float32, device=device)
-    sink = torch.empty(1, dtype=torch.float32, device=device)
+    R = max(1, min(256, int(2 * L2_BYTES // max(1, bytes_per_copy)) + 1))
+    bufs = [make() for _ in range(R)]
+    for bb in bufs[: min(R, 3)]:
+        launch(bb)
+    torch.cuda.synchronize(device)
+    reps = max(1, (min_launches + R - 1) // R)
+    method = "graph"
+    try:
+        g = torch.cuda.CUDAGraph()
+        st = torch.cuda.Stream(device)
+        with torch.cuda.stream(st):
+            for bb in bufs:
+                launch(bb)
+            torch.cuda.synchronize(device)
+            with torch.cuda.graph(g, stream=st):
+                for bb in bufs:
+                    launch(bb)
+        torch.cuda.synchronize(device)
+        g.replay()
+        torch.cuda.synchronize(device)
+
+        def run():
+            for _ in range(reps):
+                g.replay()
+    except Exception:  # noqa: BLE001 - capture unsupported: enqueue the launches directly
+        method = "stream"
+        torch.cuda.synchronize(device)
+
+        def run():
+            for _ in range(reps):
+                for bb in bufs:
+                    launch(bb)
+    a = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    a.record()
+    run()
+    e.record()
+    torch.cuda.synchronize(device)
+    return a.elapsed_time(e) / (reps * R), R, method
+
+
+def time_grid(kb_attn, peaks, prefill_batches, device):
+    """The configuration grid of the KernelBraid README ("Performance":
+    prefill at S in 1K..16K, decode at B in 1..16 x ctx in 128..8K).  Each
+    configuration is timed as back-to-back launches over rotating input copies
+    larger than L2 (rotating_launch_ms).  Returns one record per configuration."""
+    import torch
+
     gen = torch.Generator(device=device)
-
-    def timed(fn):
-        ts = []
-        for i in range(reps + 3):
-            torch.sum(flush, dim=0, keepdim=True, out=sink)
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            if i >= 3:
-                ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
-
     out = []
+
+    def randn(shape):
+        return torch.randn(shape, device=device, dtype=torch.bfloat16, generator=gen)
+
     for S in GRID_PREFILL_S:
         for B in prefill_batches:
             gen.manual_seed(8_000_000 + 100 * (S // 1024) + B)
-            q = torch.randn(B, HQ, S, D, device=device, dtype=torch.bfloat16, generator=gen)
-            k = torch.randn(B, HKV, S, D, device=device, dtype=torch.bfloat16, generator=gen)
-            v = torch.randn(B, HKV, S, D, device=device, dtype=torch.bfloat16, generator=gen)
-            o = torch.empty_like(q)
-            ms = timed(lambda: kb_attn.prefill(q, k, v, out=o))
+            per_copy = (2 * B * HQ * S + 2 * B * HKV * S) * D * 2
+            ms, R, how = rotating_launch_ms(
+                lambda: (randn((B, HQ, S, D)), randn((B, HKV, S, D)), randn((B, HKV, S, D)),
+                         torch.empty((B, HQ, S, D), device=device, dtype=torch.bfloat16)),
+                lambda t: kb_attn.prefill(t[0], t[1], t[2], out=t[3]), per_copy, device)
             tf = prefill_flops(B, S) / (ms / 1e3) / 1e12
-            out.append({"kind": "prefill", "S": S, "B": B, "ms": ms, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"]})
-            del q, k, v, o
+            out.append({"kind": "prefill", "S": S, "B": B, "ms": ms, "TFLOP/s": tf, "frac": tf / peaks["bf16_tflops"],
+                        "copies": R, "timing": how})
+            torch.cuda.empty_cache()
     for ctx in GRID_DECODE_CTX:
         for B in GRID_B:
             gen.manual_seed(9_000_000 + ctx + B)
-            q = torch.randn(B, HQ, 1, D, device=device, dtype=torch.bfloat16, generator=gen)
-            k = torch.randn(B, HKV, ctx, D, device=device, dtype=torch.bfloat16, generator=gen)
-            v = torch.randn(B, HKV, ctx, D, device=device, dtype=torch.bfloat16, generator=gen)
-            o = torch.empty_like(q)
-            ms = timed(lambda: kb_attn.decode(q, k, v, ctx, out=o))
+            per_copy = decode_bytes(B, ctx)
+            ms, R, how = rotating_launch_ms(
+                lambda: (randn((B, HQ, 1, D)), randn((B, HKV, ctx, D)), randn((B, HKV, ctx, D)),
+                         torch.empty((B, HQ, 1, D), device=device, dtype=torch.bfloat16)),
+                lambda t: kb_attn.decode(t[0], t[1], t[2], ctx, out=t[3]), per_copy, device)
             gbs = decode_bytes(B, ctx) / (ms / 1e3) / 1e9
             out.append({"kind": "decode", "ctx": ctx, "B": B, "us": ms * 1e3, "GB/s": gbs,
-                        "frac": gbs / peaks["hbm_gbs"]})
-            del q, k, v, o
+                        "frac": gbs / peaks["hbm_gbs"], "copies": R, "timing": how})
+            torch.cuda.empty_cache()
     kb_attn.check_device_status()
     return out
 
@@ -680,8 +663,10 @@ def grid_summary(records, peaks):
     dec = [r for r in records if r["kind"] == "decode"]
     return {
         "workload": ("KernelBraid README grid: prefill B=1, S in 1K/4K/8K/16K; decode B in 1/4/8/16 x ctx in 128/1K/4K/8K; "
-                     "Hq=32 Hkv=8 D=128 bf16, torch.randn inputs; L2 flushed (512 MB read) before each timed "
-                     "launch; median of the timed launches"),
+                     "Hq=32 Hkv=8 D=128 bf16, torch.randn inputs; each configuration timed over back-to-back "
+                     "launches (a CUDA graph) on rotating input copies that together exceed L2 twice over, "
+                     "so no launch finds its inputs in L2"),
+        "timing": sorted({r["timing"] for r in records}),
         "prefill_b1": {str(r["S"]): {"TFLOP/s": round(r["TFLOP/s"], 1), "frac": round(r["frac"], 4)} for r in pre},
         "decode": {f"B{r['B']}_ctx{r['ctx']}": {"GB/s": round(r["GB/s"], 1), "us": round(r["us"], 2),
                                                 "frac": round(r["frac"], 4)} for r in dec},
@@ -702,7 +687,7 @@ def run_sweep(args, local):
     from bitwise_aligned_causal_gb300 import kb_attn
 
     peaks = load_peaks()
-    for r in time_grid(kb_attn, peaks, GRID_B, args.steps, torch.device("cuda", local)):
+    for r in time_grid(kb_attn, peaks, GRID_B, torch.device("cuda", local)):
         print(json.dumps(dict(r, peak_source=peaks["source"])), flush=True)
 
 
@@ -716,7 +701,6 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip timing the training forward + backward")
-    ap.add_argument("--no-segmented", action="store_true", help="skip timing the small-batch segmented decode")
     ap.add_argument("--no-grid", action="store_true", help="skip timing the README's configuration grid")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="full")
     ap.add_argument("--sweep", action="store_true",

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkb_attn.so")
-SOURCES = ["kb_host.cu", "kb_prefill.cu", "kb_prefill2.cu", "kb_decode.cu", "kb_backward.cu", "kb_segment.cu"]
+SOURCES = ["kb_host.cu", "kb_prefill2.cu", "kb_decode.cu", "kb_backward.cu", "kb_segment.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

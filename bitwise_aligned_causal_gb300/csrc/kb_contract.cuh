@@ -5,7 +5,7 @@
 // one-token decode, so that the three produce bitwise-identical output rows
 // for the same inputs and context ("Advantages"; the "Usage" example compares
 // the raw bf16 bits).  The pages do not print the contract's contents, so it
-// is fixed here, version 2:
+// is fixed here, version 3:
 //
 //  C1 One KV tile of 128 keys, anchored at key 0, visited in ascending order
 //     0..floor(p/128) for a row at absolute position p.  Prefill/chunk query
@@ -18,12 +18,16 @@
 //     the functions below; data-dependent choices (when the reference max
 //     moves, which keys are masked) are per row only.
 //  C4 One normalisation: o = bf16_rn(O * rcp_rn(l)).
-//  C5 No split of the KV range in the default mode.  The segmented mode
-//     (opt-in, the same seg_tiles for every entry point of the mode) cuts a
-//     row's key tiles into segments of seg_tiles tiles anchored at tile 0;
-//     each segment runs C1-C3 from the fresh state (its first P V clears the
+//  C5 A fixed, length-determined split of the KV range: a row's key tiles
+//     are cut into segments of kSegTiles tiles anchored at tile 0; each
+//     segment runs C1-C3 from the fresh state (its first P V clears the
 //     accumulator) and the segments are folded left to right by fold_state /
-//     fold_o below, then C4.  One segment folds to the default mode's bits.
+//     fold_o below, then C4.  A row whose keys fit in one segment gets the
+//     plain online-softmax bits.  The segment length is the same for every
+//     entry point, so a decode may give each segment its own CTA while
+//     prefill folds the same segments in order.  (The *_seg entry points take
+//     other segment lengths; a length of at least the row's tile count is
+//     the unsplit online softmax, version 2's default.)
 //
 // Every floating-point operation below is an explicit round-to-nearest
 // intrinsic, so the compiler cannot contract or reorder them differently in
@@ -39,7 +43,8 @@ constexpr int kHeadDim = 128;      // D
 constexpr int kTileKeys = 128;     // keys per KV tile (C1)
 constexpr int kTileRows = 128;     // query rows per tile = MMA M (C2)
 constexpr int kGroup = 4;          // query heads per KV head (32 / 8)
-constexpr int kContractVersion = 2;
+constexpr int kContractVersion = 3;
+constexpr int kSegTiles = 8;       // C5: keys per segment = 8 * 128 = 1024
 
 // c = log2(e) / sqrt(128) = 0.1275174308245986852... rounded to the nearest
 // fp32, bit pattern 0x3E0293EE.  The softmax weight of score s against the
@@ -276,6 +281,37 @@ __device__ __forceinline__ FoldScale fold_state(RowState& acc, const RowState& s
 
 __device__ __forceinline__ float fold_o(float o_acc, float o_seg, FoldScale f) {
   return __fmaf_rn(o_acc, f.a, __fmul_rn(o_seg, f.b));
+}
+
+// C5 fold of one finished segment into a thread's share of the folded O, in
+// the register layout of two 16x256b.x8 TMEM loads (columns 0-63 and
+// 64-127): registers 4r, 4r+1 of each half belong to the thread's row A,
+// 4r+2, 4r+3 to its row B.  `first` takes the segment as it is.  kRowB false:
+// only row A is real (the B registers are ignored).
+template <bool kRowB>
+__device__ __forceinline__ void fold_segment_quad(uint32_t (&acc0)[32], uint32_t (&acc1)[32], RowState& accA,
+                                                  RowState& accB, const RowState& segA, const RowState& segB,
+                                                  const uint32_t (&o0)[32], const uint32_t (&o1)[32], bool first) {
+  if (first) {
+    accA = segA;
+    if (kRowB) accB = segB;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      acc0[i] = o0[i];
+      acc1[i] = o1[i];
+    }
+    return;
+  }
+  const FoldScale fA = fold_state(accA, segA);
+  FoldScale fB = fA;
+  if (kRowB) fB = fold_state(accB, segB);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (!kRowB && (i & 2)) continue;
+    const FoldScale f = (i & 2) ? fB : fA;
+    acc0[i] = __float_as_uint(fold_o(__uint_as_float(acc0[i]), __uint_as_float(o0[i]), f));
+    acc1[i] = __float_as_uint(fold_o(__uint_as_float(acc1[i]), __uint_as_float(o1[i]), f));
+  }
 }
 
 }  // namespace kb

@@ -32,6 +32,7 @@ struct DeviceState {
   uint32_t* err = nullptr;
   float* seg_scratch = nullptr;   // g_seg_scratch on this device
   int sm_count = 0;
+  int cluster_fit[4] = {0, 0, 0, 0};   // clusters of 2, 4, 8 narrow packed CTAs the device runs at once
   bool ready = false;
 };
 DeviceState g_dev[kMaxDevices];
@@ -61,6 +62,7 @@ kb_status get_device_state(DeviceState** out) {
     st.seg_scratch = static_cast<float*>(p);
     if ((e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_fail(e);
+    kb::packed_cluster_capacity(st.cluster_fit);
     st.ready = true;
   }
   if (!g_encode) {
@@ -143,8 +145,31 @@ struct Ragged {
   const int* lens = nullptr;
 };
 
+// CTAs per (sub-chunk, b, kv head) of the packed kernel's fold mode: the
+// largest cluster whose clusters all run at once (one wave), when the batch
+// alone would leave SMs idle.  Narrow rows only; the other CTAs of a cluster
+// keep their segments' partials in shared memory, so a CTA may own at most
+// as many segments as it has partial slots.
+int choose_cluster(const DeviceState& dst, int L, int n_sub, int B, int Hkv, int n_kv_max) {
+  if (L > 2) return 1;
+  const long long units = static_cast<long long>(n_sub) * B * Hkv;
+  if (2 * units > dst.sm_count) return 1;
+  const int ns = (n_kv_max + kb::kSegTiles - 1) / kb::kSegTiles;
+  const long long slots = kb::packed_partial_slots(kb::kGroup * L);
+  for (int i = 3, c = 8; i >= 1; --i, c /= 2) {
+    if (c > ns || units > dst.cluster_fit[i]) continue;
+    if ((ns + c - 1) / c > slots) continue;
+    return c;
+  }
+  return 1;
+}
+
+// seg_tiles: 0 for the default entry points (the contract's segment length,
+// folded in the kernels); > 0 for the *_seg entry points (that length; chunks
+// of at most 32 rows then leave per-segment partials in `workspace`, which a
+// second kernel folds).
 kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int L, int start,
-                     int kv_cap, int q_tiles_per_cta, void* stream, const Paging* paging = nullptr,
+                     int kv_cap, int cta_shape, void* stream, const Paging* paging = nullptr,
                      const Ragged* ragged = nullptr, float* lse = nullptr, int seg_tiles = 0,
                      void* workspace = nullptr, size_t workspace_bytes = 0) {
   kb_status s = check_ptrs(q, k, v, o);
@@ -153,19 +178,19 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   if (L < 1 || start < 0 || kv_cap < 1) return KB_ERR_INVALID_ARG;
   if (static_cast<long long>(start) + L > kv_cap) return KB_ERR_INVALID_ARG;
   if (kv_cap > kMaxRows) return KB_ERR_UNSUPPORTED;
-  if (q_tiles_per_cta < 0 || q_tiles_per_cta > kb::kShapePersistent) return KB_ERR_INVALID_ARG;
-  const bool force_persistent = (q_tiles_per_cta == kb::kShapePersistent);
-  if (force_persistent) q_tiles_per_cta = kb::kShapeOneTilePerSm;
-  if (q_tiles_per_cta == 0 && L > kb::kMaxPackedRows) return KB_ERR_INVALID_ARG;
-  if (lse != nullptr && q_tiles_per_cta != kb::kShapeOneTilePerSm) return KB_ERR_INVALID_ARG;
+  if (cta_shape != 0 && cta_shape != kb::kShapeOneTilePerSm && cta_shape != kb::kShapePersistent)
+    return KB_ERR_INVALID_ARG;
+  const bool force_persistent = (cta_shape == kb::kShapePersistent);
+  const bool packed = (cta_shape == 0);
+  if (packed && L > kb::kMaxPackedRows) return KB_ERR_INVALID_ARG;
+  if (lse != nullptr && packed) return KB_ERR_INVALID_ARG;
   if (seg_tiles < 0) return KB_ERR_INVALID_ARG;
-  if (seg_tiles > 0) {
-    // the segmented mode runs on the packed kernel (with a workspace) and the
-    // one-tile-per-SM kernel, contiguous caches, no log-sum-exp
+  const bool explicit_seg = seg_tiles > 0;
+  if (explicit_seg) {
+    // the *_seg entry points: contiguous caches, no log-sum-exp; short chunks
+    // leave their per-segment partials in the caller's workspace
     if (paging || ragged || lse) return KB_ERR_UNSUPPORTED;
-    if (q_tiles_per_cta != 0 && q_tiles_per_cta != kb::kShapeOneTilePerSm) return KB_ERR_INVALID_ARG;
-    if (q_tiles_per_cta == 0) {
-      // the packed kernel leaves per-segment partials in the caller's workspace
+    if (packed) {
       const int n_kv = (start + L - 1) / kb::kTileKeys + 1;
       const long long n_seg = (n_kv + seg_tiles - 1) / seg_tiles;
       const unsigned long long need =
@@ -175,15 +200,13 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
       if (n_seg * 2LL * B * Hkv > 0x7FFFFFFFLL) return KB_ERR_UNSUPPORTED;
     }
   }
+  const int seg = explicit_seg ? seg_tiles : kb::kSegTiles;
   // a ragged batch sizes the grid for its longest possible sequence
   const int first_tile = ragged ? 0 : start / kb::kTileRows;
   const int last_tile = ragged ? (L + kb::kTileRows - 2) / kb::kTileRows : (start + L - 1) / kb::kTileRows;
-  // CTAs: tile kernels one per (query tile, batch, head group of 1 or 2
-  // heads); packed kernel at most two per (batch, KV head)
-  const int heads_per_cta = q_tiles_per_cta == 2 ? 2 : 1;
-  const long long grid = q_tiles_per_cta > 0
-                             ? static_cast<long long>(last_tile - first_tile + 1) * B * (Hq / heads_per_cta)
-                             : 2LL * B * Hkv;
+  // CTAs: the tile kernel at most one per (query tile, batch, head); the
+  // packed kernel at most two sub-chunks x a cluster of 8 per (batch, KV head)
+  const long long grid = !packed ? static_cast<long long>(last_tile - first_tile + 1) * B * Hq : 16LL * B * Hkv;
   if (grid > 0x7FFFFFFFLL) return KB_ERR_UNSUPPORTED;
 
   DeviceState* dst = nullptr;
@@ -211,16 +234,10 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
                              row_bytes;
   if ((s = encode_rows_map(&tk, k, kv_rows, kv_planes, kv_stride)) != KB_OK) return s;
   if ((s = encode_rows_map(&tv, v, kv_rows, kv_planes, kv_stride)) != KB_OK) return s;
-  if (q_tiles_per_cta == 0) {
+  if (packed) {
     // query rows packed by GQA group
     const int split = std::min(L, kb::kTileKeys - start % kb::kTileKeys);
     const int n_sub = (ragged || split < L) ? 2 : 1;
-    int n_seg = 0;
-    if (seg_tiles > 0) {
-      const int n_kv = (start + L - 1) / kb::kTileKeys + 1;
-      n_seg = (n_kv + seg_tiles - 1) / seg_tiles;
-      if ((s = check_device_pointer(workspace)) != KB_OK) return s;
-    }
     kb::PackedArgs a{};
     a.q = q;
     a.o = o;
@@ -242,15 +259,23 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
     }
     a.err = dst->err;
     a.n_sub = n_sub;
-    if (seg_tiles > 0) {
-      a.seg_tiles = seg_tiles;
+    int n_seg = 0;
+    if (explicit_seg) {
+      const int n_kv = (start + L - 1) / kb::kTileKeys + 1;
+      n_seg = (n_kv + seg - 1) / seg;
+      if ((s = check_device_pointer(workspace)) != KB_OK) return s;
+      a.seg_tiles = seg;
       a.n_seg = n_seg;
       a.part = static_cast<float*>(workspace);
+    } else {
+      const int n_kv_max = ragged ? (kv_cap - 1) / kb::kTileKeys + 1 : (start + L - 1) / kb::kTileKeys + 1;
+      a.fold_seg = seg;
+      a.cluster = choose_cluster(*dst, L, n_sub, B, Hkv, n_kv_max);
     }
     cudaError_t e = kb::launch_packed(tk, tv, a, n_sub, static_cast<cudaStream_t>(stream));
-    if (e == cudaSuccess && seg_tiles > 0)
+    if (e == cudaSuccess && explicit_seg)
       e = kb::launch_seg_fold(static_cast<const float*>(workspace), o, static_cast<long long>(B) * Hq * L, L, start,
-                              seg_tiles, n_seg, static_cast<cudaStream_t>(stream));
+                              seg, n_seg, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return KB_OK;
   }
@@ -272,9 +297,9 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   // share K/V in L2; below that, globally longest tile first
   a.group_major = grid > 4LL * dst->sm_count ? 1 : 0;
   a.lse = lse;
-  a.seg_tiles = seg_tiles;
+  a.seg_tiles = seg;
   a.max_ctas = dst->sm_count > 0 ? dst->sm_count : 1;
-  if (q_tiles_per_cta == kb::kShapeOneTilePerSm) {
+  {
     // Persistent when what it saves beats what it costs: it hides a CTA's
     // start and end (about 5000 cycles, fitted to timings of both launches
     // from S=1.5K to 16K) under the previous unit, against a unit of (n+1)/2
@@ -302,9 +327,7 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
     a.num_pages = paging->num_pages;
   }
   a.err = dst->err;
-  const cudaError_t e = q_tiles_per_cta == kb::kShapeOneTilePerSm
-                            ? kb::launch_prefill_s2(tq, tk, tv, a, static_cast<cudaStream_t>(stream))
-                            : kb::launch_prefill(q_tiles_per_cta, tq, tk, tv, a, static_cast<cudaStream_t>(stream));
+  const cudaError_t e = kb::launch_prefill_s2(tq, tk, tv, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return KB_OK;
 }
@@ -524,6 +547,8 @@ kb_status kb_attn_decode_paged(const void* q, const void* k_pages, const void* v
   a.L = 1;
   a.ctx_lens = ctx_lens;
   a.max_ctx = pages_per_seq * page_size;
+  a.fold_seg = kb::kSegTiles;
+  a.cluster = choose_cluster(*dst, 1, 1, B, Hkv, (a.max_ctx - 1) / kb::kTileKeys + 1);
   a.block_table = block_table;
   a.pages_per_seq = pages_per_seq;
   a.page_size = page_size;

@@ -22,7 +22,7 @@ struct PrefillArgs {
   int kv_cap;              // keys per sequence the cache can hold
   int group_major;         // CTA order: 1 = (b, g) slowest, 0 = query tile slowest
   float* lse;              // optional [B, Hq, L] fp32: natural-log log-sum-exp of each row's scaled scores
-  int seg_tiles;           // C5 segmented mode: segment length in key tiles (0 = default mode)
+  int seg_tiles;           // C5 segment length in key tiles (0: the whole row is one segment)
   int max_ctas;            // CTAs of a persistent launch (one per SM)
   int persistent;          // 1: CTAs walk pairs of units; 0: one CTA per unit
   uint32_t* err;    // device error word
@@ -42,7 +42,11 @@ struct PackedArgs {
   const int* starts;       // optional device [B]: per-sequence start and row count (ragged
   const int* lens;         //   batch); L is then the row stride of q and o
   int n_sub;               // sub-chunks per (b, kv head) in the grid (1 or 2)
-  // segmented mode (seg_tiles > 0): CTA (seg, sub, b, g) runs key tiles
+  // fold mode (part == nullptr): C5 segments of fold_seg key tiles, cut into
+  // contiguous blocks over a cluster of `cluster` CTAs per (sub, b, g); the
+  // cluster's first CTA folds them all and writes o
+  int fold_seg, cluster;
+  // workspace mode (part != nullptr): CTA (seg, sub, b, g) runs key tiles
   // [seg * seg_tiles, +seg_tiles) from the fresh state and writes the rows'
   // partial (O[128], m, mc, l) to part[((b*Hq + h)*L + r)*n_seg + seg][132]
   int seg_tiles, n_seg;
@@ -54,10 +58,6 @@ constexpr int kPartFloats = 132;   // one partial: O[128], m, mc, l, pad
 
 constexpr int kMaxPackedRows = 32;   // query rows per (batch, head) the packed kernel takes
 
-// Query tiles per CTA of the prefill kernel: 1 (two CTAs per SM) or 2
-// (two heads of one GQA group share every K/V tile).
-cudaError_t launch_prefill(int q_tiles_per_cta, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const PrefillArgs& a, cudaStream_t s);
 // One 128-row query tile per CTA, one CTA per SM, three S buffers in TMEM
 // and separate Q K^T / P V issuers, so the tensor pipe works on later key
 // tiles while the softmax runs (CTA shape 3).
@@ -69,6 +69,12 @@ cudaError_t launch_prefill_s2(const CUtensorMap& tq, const CUtensorMap& tk, cons
 // n_sub: 1, or 2 when the chunk crosses a 128-position tile boundary.
 cudaError_t launch_packed(const CUtensorMap& tk, const CUtensorMap& tv, const PackedArgs& a, int n_sub,
                           cudaStream_t s);
+// Partials a CTA of the narrow packed kernel can keep in shared memory for
+// the cluster's first CTA, with n_rows packed rows.
+uint32_t packed_partial_slots(int n_rows);
+// Clusters of 2, 4 and 8 CTAs (entries 1, 2, 3) of the narrow packed kernel
+// the current device runs at once; entry 0 is unused.
+void packed_cluster_capacity(int (&active)[4]);
 // Gradient of a whole-sequence causal prefill (query row i at position i).
 struct BwdArgs {
   const void* o;           // [B, Hq, S, 128] bf16 forward output

@@ -97,6 +97,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// mbar_wait for a role that is not on the critical path: between polls the
+// warp sleeps for about `sleep_ns`, so it does not take issue slots from the
+// warps of its SM sub-partition that are.  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                               uint32_t* err, uint32_t code, uint32_t sleep_ns) {
+  const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (*(volatile uint32_t*)err != 0) { *abort_flag = 1; return false; }
+    if (global_timer_ns() - t0 > KB_WAIT_LIMIT_NS) {
+      atomicCAS(err, 0u, code);
+      *abort_flag = 1;
+      return false;
+    }
+    __nanosleep(sleep_ns);
+  }
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
@@ -140,6 +160,14 @@ __device__ __forceinline__ void tma_load_tile_hint(uint32_t dst, const void* tma
       " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(row), "r"(0), "r"(plane), "r"(bar),
         "l"(policy)
+      : "memory");
+}
+
+// Prefetch one whole 128-row tile (addressed as tma_load_tile) into L2 only.
+__device__ __forceinline__ void tma_prefetch_tile_l2(const void* tmap, int row, int plane) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+      ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(row), "r"(0), "r"(plane)
       : "memory");
 }
 
@@ -248,6 +276,38 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
       : KB_R8(0), KB_R8(8), KB_R8(16), KB_R8(24)
       : "r"(taddr)
       : "memory");
+}
+
+// 16 consecutive columns.
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : KB_R8(0), KB_R8(8)
+      : "r"(taddr)
+      : "memory");
+}
+
+// 16 consecutive columns, issued without waiting: the registers hold the
+// data only after tmem_ld16_wait_for on the same array.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : KB_R8(0), KB_R8(8)
+      : "r"(taddr)
+      : "memory");
+}
+
+// Wait for every TMEM load this thread issued; the array is an in/out
+// operand, so no use of it can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld16_wait_for(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
 }
 
 // 64 consecutive columns, two loads then one wait.
@@ -457,5 +517,105 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 }
 
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0; }
+
+// ------------------------------------------------------ register reallocation
+// Every warp of a warpgroup executes the same setmaxnreg; the counts of all
+// warpgroups must add up to no more than the registers the CTA was launched
+// with (threads x registers per thread at launch).
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+// ------------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Cluster-wide barrier: every thread of every CTA of the cluster arrives
+// (release: its shared-memory writes become visible to the other CTAs) and
+// waits (acquire).  Like __syncthreads, it completes once all have arrived.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// The two halves of cluster_sync, for a barrier whose wait comes later.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
+// Arrive on an mbarrier of another CTA of the cluster (address from
+// smem_addr_in_cta), releasing this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
+// try_wait on this CTA's mbarrier, acquiring what other CTAs of the cluster
+// released before arriving on it.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait (as mbar_wait) for arrivals from other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                                  uint32_t* err, uint32_t code) {
+  const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (*(volatile uint32_t*)err != 0) { *abort_flag = 1; return false; }
+    if (global_timer_ns() - t0 > KB_WAIT_LIMIT_NS) {
+      atomicCAS(err, 0u, code);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32x4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t smem_addr_in_cta(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 
 }  // namespace kb

@@ -16,6 +16,16 @@
  * kb_attn_prefill, by kb_attn_chunk (any split of the sequence) and by
  * kb_attn_decode (ctx_len = p + 1) has the same bf16 bits.
  *
+ * Contract version 3 (kb_contract_version): key tiles of 128 keys visited in
+ * ascending order; one tcgen05 MMA shape and k-order; one per-row online
+ * softmax (fp32 max and sum, one exp2 path, scale 1/sqrt(128)); one final
+ * normalisation; and a fixed, length-determined split of every row's keys
+ * into segments of 1024 keys (8 tiles) anchored at key 0, each segment run
+ * from the fresh softmax state and the segments folded left to right by one
+ * fold function.  The split lets a small-batch decode of a long context run
+ * its segments on several SMs at once while prefill folds the same segments
+ * in order, so both stay bit-identical.
+ *
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers on the current CUDA device,
  *    bf16, contiguous, 16-byte aligned, owned by the caller.  The library
@@ -171,15 +181,17 @@ kb_status kb_attn_check_device_status(void* stream);
 kb_status kb_attn_debug_wait_timeout(int limit_us, void* stream);
 
 /*
- * Segmented mode (contract C5: a fixed, length-determined split of the KV range):
- * a row's key tiles are cut into segments of seg_tiles 128-key tiles anchored
- * at key 0; each segment runs the default mode's tile steps from the fresh
- * state and the segments are folded left to right by one fold function, then
- * normalised.  Every entry point of the mode gives the same bits for a row
- * at position p when called with the same seg_tiles (>= 1); a row whose keys
- * fit in one segment has the default mode's bits.  The split lets a decode
- * of a long context run one CTA per segment (small batches), at the price of
- * an extra fold for prefill.
+ * Explicit segment length (contract C5 with seg_tiles instead of 8): a row's
+ * key tiles are cut into segments of seg_tiles 128-key tiles anchored at key
+ * 0; each segment runs the tile steps from the fresh state and the segments
+ * are folded left to right by the contract's fold function, then normalised.
+ * Every entry point below gives the same bits for a row at position p when
+ * called with the same seg_tiles (>= 1).  seg_tiles = 8 gives the default
+ * entry points' bits; a seg_tiles of at least the row's tile count is the
+ * unsplit online softmax (contract version 2's default).  These calls run a
+ * different fold path from the default entry points (short chunks write
+ * per-segment partials to a workspace that a second kernel folds), so with
+ * seg_tiles = 8 they also cross-check the default path's bits.
  *
  * kb_attn_prefill_seg: as kb_attn_prefill (no workspace).
  * kb_attn_chunk_seg:   as kb_attn_chunk.  Chunks of at most 32 rows (and
@@ -261,15 +273,15 @@ kb_status kb_attn_backward(const void* q, const void* k, const void* v, const vo
 
 /*
  * Prefill/chunk with an explicit kernel shape, for tests of the contract:
- * q_tiles_per_cta = 1 or 2 runs the tile kernel with that many 128-row query
- * tiles per CTA; 3 runs the tile kernel with one query tile per CTA, one CTA
- * per SM and three score buffers (Q K^T of later key tiles overlaps the
- * softmax of the current one), launched persistent (CTAs walk balanced pairs
- * of query tiles) or one CTA per tile as the sizes suit; 4 is 3 with the
- * persistent launch forced; 0 runs the packed kernel (the 4 heads of a GQA group times
- * the chunk's rows in one MMA tile; L <= 32).  kb_attn_chunk, kb_attn_prefill
- * and kb_attn_decode pick packed for L <= 32 and 3 otherwise.  Every shape
- * gives the same bits.
+ * q_tiles_per_cta = 3 runs the tile kernel (one 128-row query tile per CTA,
+ * one CTA per SM, three score buffers, so Q K^T of later key tiles overlaps
+ * the softmax of the current one), launched persistent (CTAs walk balanced
+ * pairs of query tiles) or one CTA per tile as the sizes suit; 4 is 3 with
+ * the persistent launch forced; 0 runs the packed kernel (the 4 heads of a
+ * GQA group times the chunk's rows in one MMA tile; L <= 32).  Other values
+ * return KB_ERR_INVALID_ARG.  kb_attn_chunk, kb_attn_prefill and
+ * kb_attn_decode pick packed for L <= 32 and 3 otherwise.  Every shape gives
+ * the same bits.
  */
 kb_status kb_attn_chunk_cta_shape(const void* q, const void* k, const void* v, void* o,
                                   int B, int Hq, int Hkv, int L, int start, int kv_cap,

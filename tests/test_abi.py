@@ -46,7 +46,7 @@ def test_status_strings_and_version(kb):
     assert kb.kb_status_string(0) == "ok"
     assert "timed out" in kb.kb_status_string(4)
     assert kb.kb_status_string(99) == "unknown status"
-    assert kb.kb_contract_version() == 2
+    assert kb.kb_contract_version() == 3
 
 
 FAKE = 0x1000_0000     # aligned, non-null; never dereferenced by the host checks below
@@ -75,7 +75,8 @@ def test_bad_sizes_rejected(kb):
     # decode context within the cache
     assert kb.kb_attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 11, 10) == kb.KB_ERR_INVALID_ARG
     assert kb.kb_attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 0, 10) == kb.KB_ERR_INVALID_ARG
-    assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 4, 0, 10, 5) == kb.KB_ERR_INVALID_ARG
+    for shape in (1, 2, 5, -1):          # the tile kernel (3, 4) and the packed kernel (0) only
+        assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 4, 0, 10, shape) == kb.KB_ERR_INVALID_ARG
     assert kb.kb_attn_debug_wait_timeout(0) == kb.KB_ERR_INVALID_ARG
 
 

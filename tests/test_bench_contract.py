@@ -57,14 +57,11 @@ def test_gpu_arm_line_keys_and_arithmetic():
 
 
 def test_gpu_arm_optional_objects():
-    d = _emit(bwd={"bwd_ms": 28.0, "bwd_ms_local": 28.0, "fwd_ms": 6.0, "reps": 10},
-              seg={"default_ms": 0.08, "seg_ms": 0.02, "reps": 20})
+    d = _emit(bwd={"bwd_ms": 28.0, "bwd_ms_local": 28.0, "fwd_ms": 6.0, "reps": 10})
     pf = bench.prefill_flops(bench.PREFILL_B, bench.PREFILL_S)
     assert d["backward"]["value"] == pytest.approx(2.5 * pf / 28.0e-3 / 1e12)
     assert d["backward"]["roofline"]["frac"] == pytest.approx(d["backward"]["roofline"]["achieved"] /
                                                               d["backward"]["roofline"]["peak"])
-    small = d["decode_small_batch"]
-    assert small["segmented"]["us"] == pytest.approx(20.0) and small["default"]["us"] == pytest.approx(80.0)
 
 
 def test_reference_arm_line():
@@ -88,9 +85,9 @@ def test_reference_arm_line():
 
 def test_grid_summary_reports_both_bars():
     peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 8000.0, "source": "measured"}
-    recs = [{"kind": "prefill", "S": S, "B": 1, "ms": 1.0, "TFLOP/s": 1000.0, "frac": 0.5}
+    recs = [{"kind": "prefill", "S": S, "B": 1, "ms": 1.0, "TFLOP/s": 1000.0, "frac": 0.5, "timing": "graph"}
             for S in bench.GRID_PREFILL_S]
-    recs += [{"kind": "decode", "ctx": c, "B": b, "us": 10.0, "GB/s": 4000.0, "frac": 0.5}
+    recs += [{"kind": "decode", "ctx": c, "B": b, "us": 10.0, "GB/s": 4000.0, "frac": 0.5, "timing": "graph"}
              for c in bench.GRID_DECODE_CTX for b in bench.GRID_B]
     g = bench.grid_summary(recs, peaks)
     assert len(g["prefill_b1"]) == 4 and len(g["decode"]) == 16

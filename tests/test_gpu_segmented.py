@@ -1,11 +1,12 @@
-"""Segmented mode (contract C5): a fixed split of each row's key tiles into
-segments of seg_tiles tiles, folded left to right.
+"""Explicit segment lengths (contract C5 with seg_tiles tiles instead of the
+contract's 8): a fixed split of each row's key tiles, folded left to right.
 
-Within the mode every entry point must give the same bits for a row
+For one segment length every entry point must give the same bits for a row
 (KernelBraid README, "Method" and "Advantages": one contract for prefill,
-partitioned forward and decode), a row that fits in one segment must give
-the default mode's bits (one segment folds to itself), and results must
-match the fp64 oracle within the forward tolerance.
+partitioned forward and decode); the contract's own length (8 tiles) must
+give the default entry points' bits; a row that fits in one segment is the
+unsplit online softmax; and results must match the fp64 oracle within the
+forward tolerance.
 """
 
 import numpy as np
@@ -49,19 +50,30 @@ def test_prefill_seg_against_oracle(kb, oracle_mod, seq, seg):
     assert_close_to_oracle(gather_rows(out, rows), want, f"prefill_seg seg={seg}")
 
 
-def test_one_segment_is_the_default_mode(kb, seq):
+def test_contract_segment_length_is_the_default_mode(kb, seq):
+    """seg_tiles = 8 is the contract's own split: prefill_seg, decode_seg and
+    chunk_seg at 8 (the workspace fold path) give the default entry points'
+    bits, and a row whose keys fit in one segment is the unsplit online
+    softmax whatever the segment length."""
     x, q, k, v = seq
-    n_tiles = (x.q.shape[2] + 127) // 128
-    a = from_dev(kb.prefill_seg(q, k, v, n_tiles))
-    b = from_dev(kb.prefill(q, k, v))
+    S = x.q.shape[2]
+    n_tiles = (S + 127) // 128
+    default = from_dev(kb.prefill(q, k, v))
+    a = from_dev(kb.prefill_seg(q, k, v, 8))
     kb.check_device_status()
-    assert np.array_equal(a, b)
-    # rows of the first segment agree for any segment length
+    assert np.array_equal(a, default)
+    unsplit = from_dev(kb.prefill_seg(q, k, v, n_tiles))
+    assert np.array_equal(unsplit[:, :, :1024], default[:, :, :1024])     # rows of one 8-tile segment
     c = from_dev(kb.prefill_seg(q, k, v, 3))
-    assert np.array_equal(c[:, :, :384], b[:, :, :384])
-    for pos in (0, 127, 383, 1499):
-        d = from_dev(kb.decode_seg(q[:, :, pos:pos + 1].contiguous(), k, v, pos + 1, n_tiles))
-        assert np.array_equal(d[:, :, 0], b[:, :, pos]), pos
+    assert np.array_equal(c[:, :, :384], unsplit[:, :, :384])             # rows of one 3-tile segment
+    for pos in (0, 127, 1023, 1024, 1499):
+        d = from_dev(kb.decode_seg(q[:, :, pos:pos + 1].contiguous(), k, v, pos + 1, 8))
+        e = from_dev(kb.decode(q[:, :, pos:pos + 1].contiguous(), k, v, pos + 1))
+        assert np.array_equal(d[:, :, 0], default[:, :, pos]), pos
+        assert np.array_equal(e[:, :, 0], default[:, :, pos]), pos
+        f = from_dev(kb.decode_seg(q[:, :, pos:pos + 1].contiguous(), k, v, pos + 1, n_tiles))
+        assert np.array_equal(f[:, :, 0], unsplit[:, :, pos]), pos
+    kb.check_device_status()
 
 
 @pytest.mark.parametrize("seg", [1, 3])

@@ -81,7 +81,7 @@ def test_ragged_persistent_launch(kb):
     """With 8 query heads the default kernel's persistent launch (CTAs walking
     pairs of query tiles) runs this ragged batch, whose shorter sequences
     leave holes in the pair schedule; each sequence must still give the bits
-    of the two-CTA tile kernel run on it alone."""
+    of the tile kernel launched one CTA per query tile, run on it alone."""
     import torch
 
     starts, lens, L_max, cap = [0, 129, 700, 3], [300, 200, 124, 1], 300, 1000
@@ -98,7 +98,7 @@ def test_ragged_persistent_launch(kb):
     for b in range(B):
         e = starts[b] + lens[b]
         ref = from_dev(kb.chunk(q[b:b + 1, :, :lens[b]].contiguous(), k[b:b + 1, :, :e].contiguous(),
-                                v[b:b + 1, :, :e].contiguous(), starts[b], q_tiles_per_cta=1))
+                                v[b:b + 1, :, :e].contiguous(), starts[b], q_tiles_per_cta=3))
         assert np.array_equal(out[b:b + 1, :, :lens[b]], ref), b
     kb.check_device_status()
 
