@@ -48,9 +48,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the sources differ from that hash, the figure no longer describes the timed
 # build and the bench line reports traffic as null.
 NCU_TRAFFIC = {
-    "prefill": {"bytes": 805.67e6 + 504.21e6, "sources": "668249ed6242cbc1",
+    "prefill": {"bytes": 805.80e6 + 503.86e6, "sources": "631e5448fef93f55",
                 "profile": "profiles/launch_list_bench_full.md"},
-    "decode": {"bytes": 537.09e6 + 0.31e6, "sources": "7b24ac5fd7482677",
+    "decode": {"bytes": 537.10e6 + 0.24e6, "sources": "2558bb14bb28d38b",
                "profile": "profiles/launch_list_bench_full.md"},
 }
 KERNEL_SOURCES = {

@@ -466,7 +466,7 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       int js = 0;                                                   // tile index within its segment
       for (int j = 0; j < n_kv && ok; ++j, ++T) {
         const int sb = T % Cfg::kSBufs;
-        ok = mbar_wait(bar(Cfg::kBarSFull + sb), (T / Cfg::kSBufs) & 1, abort_flag, args.err, kDevTimeoutMma);
+        ok = mbar_wait_spin(bar(Cfg::kBarSFull + sb), (T / Cfg::kSBufs) & 1, abort_flag, args.err, kDevTimeoutMma);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();

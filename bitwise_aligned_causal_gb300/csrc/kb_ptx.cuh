@@ -74,6 +74,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity.  On timeout (or when
 // another role of this CTA, or another CTA, already gave up) it records
 // `code` in *err and returns false.  `abort_flag` is a CTA-shared word.
@@ -95,6 +108,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       return false;
     }
   }
+}
+
+// mbar_wait for a wait on the critical path that is usually short: it first
+// polls with test_wait, which never suspends the thread, so the thread goes
+// on the moment the phase completes; then it falls back to mbar_wait.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                               uint32_t* err, uint32_t code) {
+#pragma unroll 1
+  for (int i = 0; i < 4096; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  return mbar_wait(bar, parity, abort_flag, err, code);
 }
 
 // mbar_wait for a role that is not on the critical path: between polls the
