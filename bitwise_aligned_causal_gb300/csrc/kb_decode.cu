@@ -36,8 +36,10 @@
 //    which reads the segment's O.  The cluster's first CTA folds its own
 //    segments as they finish, in registers.  The others write each segment's
 //    partial (O, m, mc, l) into the first CTA's shared memory and arrive on
-//    its barrier; the first CTA then folds them in segment order from its
-//    own shared memory and normalises.  When the partials do not fit there
+//    its barrier; the first CTA's fold warp writes its own folded segments
+//    into the slot after them and arrives too, and warps 0-3 of that CTA
+//    (their roles are over by then) fold the slots in segment order, 16
+//    threads per row, and normalise.  When the partials do not fit there
 //    (very long contexts), each CTA keeps its own and the first one reads
 //    them through distributed shared memory after a cluster barrier.  Narrow
 //    rows only take C > 1; wide chunks run C = 1 with the folded O in TMEM.
@@ -83,7 +85,11 @@ struct PackedCfg {
   static constexpr int kBarStEmpty = kBarStFull + 1;       // narrow: ... and read by the fold warp
   static constexpr int kBarPart = kBarStEmpty + 1;         // first CTA of a cluster: every partial written
   static constexpr int kBarDrain = kBarPart + 1;           // 2: one per MMA issuer
-  static constexpr int kNumBars = kBarDrain + 2;
+  static constexpr int kBarQReady = kBarDrain + 2;         // Q written to shared memory by its loaders
+  static constexpr int kNumBars = kBarQReady + 1;
+  // Q is loaded by the softmax warps (and the fold warp when narrow) while
+  // the producers' first K/V loads are already in flight
+  static constexpr int kQLoaders = 32 * (kSoftmaxWarps + (kWide ? 0 : 1));
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kStatsOff = kMiscOff + 16u;      // narrow: float2 (m, l) of rows 0..7
   // narrow: the rest of shared memory holds the segment partials a
@@ -212,42 +218,25 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   const int tail_from = seq_kv - (n_kv - 1) * kTileKeys;   // first V row of the last tile past the sequence
   const uint32_t slot_bytes = static_cast<uint32_t>(n_rows) * kPartFloats * 4u;
   // fold mode, C > 1: the other CTAs' segments (from s_first on) go to the
-  // first CTA's shared memory when they fit there ("push"); otherwise each
-  // CTA keeps its own and the first CTA reads them remotely
+  // first CTA's shared memory, followed by the first CTA's own folded
+  // segments, when they fit there ("push"); otherwise each CTA keeps its own
+  // and the first CTA reads them remotely
   const int s_first = seg_block_start(1, ns, C);
   const bool push = C > 1 && !ws_mode &&
-                    static_cast<uint32_t>(ns - s_first) * slot_bytes <= static_cast<uint32_t>(Cfg::kPartBytes);
+                    static_cast<uint32_t>(ns - s_first + 1) * slot_bytes <= static_cast<uint32_t>(Cfg::kPartBytes);
 
-  // Q: packed row m = head i * Lc + rr holds q[b, 4g+i, r0+rr]; unused rows
-  // are zero.  Written in the 128-byte swizzled layout the MMA descriptor
-  // expects (16-byte chunk c of row m sits at chunk c ^ (m % 8)).
-  for (int idx = threadIdx.x; idx < Cfg::kQRows * 16; idx += Cfg::kThreads) {
-    const int m = idx >> 4;
-    const int c = idx & 15;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (active && m < n_rows) {
-      const int i = m / Lc;
-      const int r = r0 + m % Lc;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          static_cast<const __nv_bfloat16*>(args.q) +
-          ((static_cast<size_t>(b) * args.Hq + g * kGroup + i) * args.L + r) * kHeadDim);
-      val = __ldg(src + c);
-    }
-    *reinterpret_cast<uint4*>(smem + Cfg::kQOff + (c >> 3) * Cfg::kQSlab + (m >> 3) * 1024 + (m & 7) * 128 +
-                              (((c & 7) ^ (m & 7)) << 4)) = val;
-  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::kNumBars; ++i) {
       uint32_t count = ((i >= Cfg::kBarPFull && i < Cfg::kBarPFull + Cfg::kSBufs) || i == Cfg::kBarORead ||
                         i == Cfg::kBarStFull || i == Cfg::kBarStEmpty)
                            ? static_cast<uint32_t>(32 * Cfg::kSoftmaxWarps) : 1u;
-      if (i == Cfg::kBarPart && C > 1) count = static_cast<uint32_t>(32 * (C - 1));   // the others' fold warps
+      if (i == Cfg::kBarPart && C > 1) count = static_cast<uint32_t>(32 * C);   // every fold warp of the cluster
+      if (i == Cfg::kBarQReady) count = static_cast<uint32_t>(Cfg::kQLoaders);
       mbar_init(bar(i), count);
     }
-    misc[1] = (*reinterpret_cast<volatile uint32_t*>(args.err) != 0) ? 1u : 0u;
+    misc[1] = 0u;
     fence_mbar_init();
   }
-  fence_proxy_async_smem();   // generic-proxy Q writes -> visible to the tensor core
   if (warp == Cfg::kQkWarp) {
     tmem_alloc(sbase + Cfg::kMiscOff, Cfg::kTmemCols);
     tmem_relinquish();
@@ -256,10 +245,39 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
-  const bool run = active && (*abort_flag == 0);
+  // Nothing global is read before this point, so the producers' first loads
+  // leave at once.  Each role reads the error word when it starts (the
+  // producers once their first loads are in flight) and skips its work if
+  // an earlier kernel recorded an error.
+  const bool run = active;
   // every CTA of the cluster has initialised its barriers once this barrier
   // completes; its wait comes before any access to another CTA
   if (C > 1) cluster_arrive();
+
+  const bool q_loader = warp < Cfg::kSoftmaxWarps || warp == Cfg::kFoldWarp;
+  if (q_loader) {
+    // Q: packed row m = head i * Lc + rr holds q[b, 4g+i, r0+rr]; unused rows
+    // are zero.  Written in the 128-byte swizzled layout the MMA descriptor
+    // expects (16-byte chunk c of row m sits at chunk c ^ (m % 8)).
+    const int t = warp == Cfg::kFoldWarp ? 32 * Cfg::kSoftmaxWarps + lane : static_cast<int>(threadIdx.x);
+    for (int idx = t; idx < Cfg::kQRows * 16; idx += Cfg::kQLoaders) {
+      const int m = idx >> 4;
+      const int c = idx & 15;
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (active && m < n_rows) {
+        const int i = m / Lc;
+        const int r = r0 + m % Lc;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(args.q) +
+            ((static_cast<size_t>(b) * args.Hq + g * kGroup + i) * args.L + r) * kHeadDim);
+        val = __ldg(src + c);
+      }
+      *reinterpret_cast<uint4*>(smem + Cfg::kQOff + (c >> 3) * Cfg::kQSlab + (m >> 3) * 1024 + (m & 7) * 128 +
+                                (((c & 7) ^ (m & 7)) << 4)) = val;
+    }
+    fence_proxy_async_smem();   // generic-proxy Q writes -> visible to the tensor core
+    mbar_arrive(bar(Cfg::kBarQReady));
+  }
 
   if (warp == Cfg::kKProdWarp || warp == Cfg::kVProdWarp) {
     // ----------------------------------------------------------- producers
@@ -280,7 +298,8 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const uint32_t use = jj / Cfg::kStages;
         int row = 0, plane = 0;
         if (lane == 0) kv_tile_coords(args, b, g, j0 + jj, row, plane);
-        if (jj >= Cfg::kStages)
+        if (jj == Cfg::kStages) ok = no_error(args.err, abort_flag);   // the first loads are in flight
+        if (ok && jj >= Cfg::kStages)
           ok = mbar_wait(bar(empty0 + slot), (use - 1) & 1, abort_flag, args.err, kDevTimeoutSlot);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -290,6 +309,8 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
         issued = jj + 1;
       }
+      if (ok && nt <= Cfg::kStages) ok = no_error(args.err, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
       if (ok && is_v && zero_tail && has_last) {
         // V rows past the sequence in its last tile may hold anything (another
         // sequence's data, NaN): make them zero so P = 0 contributes nothing.
@@ -325,7 +346,8 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     // P(j-n) out of that buffer.
     if (lane == 0 && run) {
       const uint32_t q_saddr = sbase + Cfg::kQOff;
-      bool ok = true;
+      bool ok = no_error(args.err, abort_flag) &&
+                mbar_wait(bar(Cfg::kBarQReady), 0, abort_flag, args.err, kDevTimeoutTma);
       for (int j = 0; j < nt && ok; ++j) {                  // j: tile j0 + j
         const int slot = j % Cfg::kStages;
         const int sb = j % Cfg::kSBufs;
@@ -356,7 +378,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     if (lane == 0 && run) {
       int F = 0;                                            // segments started
       int js = 0;                                           // tile index within its segment (j0 starts one)
-      bool ok = true;
+      bool ok = no_error(args.err, abort_flag);
       for (int j = 0; j < nt && ok; ++j) {                  // j: tile j0 + j
         const int slot = j % Cfg::kStages;
         const int sb = j % Cfg::kSBufs;
@@ -399,7 +421,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     RowState st = row_state_init(), prev = st, acc = st;
     int nfin = 0;                                      // segments finished (and folded into O_acc)
     int js = 0;                                        // tile index within its segment (j0 starts one)
-    bool ok = run;
+    bool ok = run && no_error(args.err, abort_flag);
     for (int j = 0; j < nt && ok; ++j) {               // j: tile j0 + j
       ok = mbar_wait(bar(Cfg::kBarSFull + j % Cfg::kSBufs), (j / Cfg::kSBufs) & 1, abort_flag, args.err,
                      kDevTimeoutMma);
@@ -556,7 +578,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     RowState acc = row_state_init();
     uint32_t acc0[32], acc1[32];                       // folded O (first CTA of the cluster)
     int nfin = 0;                                      // segments this CTA finished
-    bool ok = run;
+    bool ok = run && no_error(args.err, abort_flag);
     const bool pushing = push && rank > 0;
     // the first CTA's partial slots and barrier, as addresses of the cluster
     const uint32_t lead_slots = pushing ? smem_addr_in_cta(sbase + Cfg::kPartOff, 0u) : 0u;
@@ -647,30 +669,23 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       // them after this barrier
       if (!push) cluster_sync();
     }
-    if (ok && push && rank == 0) {
-      // every other CTA's segments are in this CTA's slots, in segment order
-      ok = mbar_wait_cluster(bar(Cfg::kBarPart), 0, abort_flag, args.err, kDevTimeoutSoftmax);
-      ok = __all_sync(0xffffffffu, ok);
-#pragma unroll 1
-      for (int sgi = s_first; sgi < ns && ok; ++sgi) {
-        const float* slot = reinterpret_cast<const float*>(smem + Cfg::kPartOff +
-                                                           static_cast<uint32_t>(sgi - s_first) * slot_bytes);
-        if (row_used) {
-          const float4 sv = *reinterpret_cast<const float4*>(slot + n_rows * 128 + 4 * m);
-          const FoldScale f = fold_state(acc, RowState{sv.x, sv.y, sv.z});
+    if (push && rank == 0) {
+      // this CTA's folded segments go to the slot after the pushed ones; warps
+      // 0-3 fold the slots once every fold warp of the cluster has arrived
+      if (ok && row_used) {
+        float* slot = reinterpret_cast<float*>(smem + Cfg::kPartOff + static_cast<uint32_t>(ns - s_first) * slot_bytes);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float2 a = *reinterpret_cast<const float2*>(slot + m * 128 + 8 * q + 2 * u);
-            const float2 c2 = *reinterpret_cast<const float2*>(slot + m * 128 + 64 + 8 * q + 2 * u);
-            acc0[4 * q] = __float_as_uint(fold_o(__uint_as_float(acc0[4 * q]), a.x, f));
-            acc0[4 * q + 1] = __float_as_uint(fold_o(__uint_as_float(acc0[4 * q + 1]), a.y, f));
-            acc1[4 * q] = __float_as_uint(fold_o(__uint_as_float(acc1[4 * q]), c2.x, f));
-            acc1[4 * q + 1] = __float_as_uint(fold_o(__uint_as_float(acc1[4 * q + 1]), c2.y, f));
-          }
+        for (int q = 0; q < 8; ++q) {
+          *reinterpret_cast<float2*>(slot + m * 128 + 8 * q + 2 * u) =
+              make_float2(__uint_as_float(acc0[4 * q]), __uint_as_float(acc0[4 * q + 1]));
+          *reinterpret_cast<float2*>(slot + m * 128 + 64 + 8 * q + 2 * u) =
+              make_float2(__uint_as_float(acc1[4 * q]), __uint_as_float(acc1[4 * q + 1]));
         }
+        if (u == 0) *reinterpret_cast<float4*>(slot + n_rows * 128 + 4 * m) = make_float4(acc.m, acc.mc, acc.l, 0.0f);
       }
+      mbar_arrive(bar(Cfg::kBarPart));                 // whatever happened, so warps 0-3 never wait for it
     }
-    if (ok && !ws_mode && rank == 0) {
+    if (ok && !ws_mode && rank == 0 && !push) {
       // fold the other CTAs' segments, in segment order, from their shared
       // memory; the next segment's partial is loaded while this one folds
       int cr = 1;                                        // rank holding the segment being loaded
@@ -748,7 +763,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     RowState st = row_state_init();
     int js = 0;                                        // tile index within its segment (j0 starts one)
     int G = 0;                                         // segments handed to the fold warp
-    bool ok = run;
+    bool ok = run && no_error(args.err, abort_flag);
     for (int j = 0; j < nt && ok; ++j) {                    // j: tile j0 + j
       ok = mbar_wait(bar(Cfg::kBarSFull + j % Cfg::kSBufs), (j / Cfg::kSBufs) & 1, abort_flag, args.err,
                      kDevTimeoutMma);
@@ -818,6 +833,55 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     if (C > 1) {
       cluster_wait();
       if (!push) cluster_sync();
+    }
+  }
+
+  if (push && rank == 0 && warp < 4) {
+    // ------------------------------- final fold of a push cluster (narrow)
+    // Slots 0 .. ns-s_first-1 hold segments s_first .. ns-1, the slot after
+    // them this CTA's folded segments 0 .. s_first-1.  Thread t folds packed
+    // row t/16, columns 8(t%16) .. +7, left to right (C5), then C4; the
+    // operations and their order are those of the fold warp's serial fold.
+    const int r = threadIdx.x >> 4;
+    const int cb = threadIdx.x & 15;
+    bool ok = mbar_wait_cluster(bar(Cfg::kBarPart), 0, abort_flag, args.err, kDevTimeoutSoftmax);
+    ok = ok && (*abort_flag == 0);
+    if (ok && r < n_rows) {
+      const float* slots = reinterpret_cast<const float*>(smem + Cfg::kPartOff);
+      const uint32_t slot_floats = slot_bytes / 4u;
+      const int n_push = ns - s_first;
+      auto load = [&](int k, float4& st, float4& oa, float4& ob) {
+        const float* sl = slots + static_cast<uint32_t>(k) * slot_floats;
+        st = *reinterpret_cast<const float4*>(sl + n_rows * 128 + 4 * r);
+        oa = *reinterpret_cast<const float4*>(sl + r * 128 + 8 * cb);
+        ob = *reinterpret_cast<const float4*>(sl + r * 128 + 8 * cb + 4);
+      };
+      float4 st, oa, ob;
+      load(n_push, st, oa, ob);
+      RowState acc{st.x, st.y, st.z};
+      float o[8] = {oa.x, oa.y, oa.z, oa.w, ob.x, ob.y, ob.z, ob.w};
+      float4 nst, noa, nob;
+      if (n_push > 0) load(0, nst, noa, nob);
+#pragma unroll 1
+      for (int k = 0; k < n_push; ++k) {
+        const float4 cst = nst, coa = noa, cob = nob;
+        if (k + 1 < n_push) load(k + 1, nst, noa, nob);           // next slot in flight while this one folds
+        const FoldScale f = fold_state(acc, RowState{cst.x, cst.y, cst.z});
+        const float os[8] = {coa.x, coa.y, coa.z, coa.w, cob.x, cob.y, cob.z, cob.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = fold_o(o[i], os[i], f);
+      }
+      const float inv_l = row_inv_l(acc);
+      const int head = r / Lc;
+      const int rr = r0 + r % Lc;
+      uint4 packed;
+      packed.x = pack_bf16x2(__fmul_rn(o[0], inv_l), __fmul_rn(o[1], inv_l));
+      packed.y = pack_bf16x2(__fmul_rn(o[2], inv_l), __fmul_rn(o[3], inv_l));
+      packed.z = pack_bf16x2(__fmul_rn(o[4], inv_l), __fmul_rn(o[5], inv_l));
+      packed.w = pack_bf16x2(__fmul_rn(o[6], inv_l), __fmul_rn(o[7], inv_l));
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.o) +
+                                ((static_cast<size_t>(b) * args.Hq + g * kGroup + head) * args.L + rr) * kHeadDim +
+                                8 * cb) = packed;
     }
   }
 

@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "../../include/kb_attn.h"
 #include "kb_contract.cuh"
@@ -32,6 +33,7 @@ struct DeviceState {
   uint32_t* err = nullptr;
   float* seg_scratch = nullptr;   // g_seg_scratch on this device
   int sm_count = 0;
+  long long l2_bytes = 0;
   int cluster_fit[4] = {0, 0, 0, 0};   // clusters of 2, 4, 8 narrow packed CTAs the device runs at once
   bool ready = false;
 };
@@ -62,6 +64,9 @@ kb_status get_device_state(DeviceState** out) {
     st.seg_scratch = static_cast<float*>(p);
     if ((e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
       return cuda_fail(e);
+    int l2 = 0;
+    if ((e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess) return cuda_fail(e);
+    st.l2_bytes = l2;
     kb::packed_cluster_capacity(st.cluster_fit);
     st.ready = true;
   }
@@ -76,6 +81,20 @@ kb_status get_device_state(DeviceState** out) {
   }
   *out = &st;
   return KB_OK;
+}
+
+// Key tiles of the busiest CTA under the tile kernel's snake schedule: units
+// of n, n-1, ..., 1 key tiles (`per_len` units of each length), longest
+// first, dealt to CTAs 0..G-1 and back.  The work is n * per_len steps.
+long long snake_max_tiles(long long n, long long per_len, long long G) {
+  static thread_local std::vector<long long> load;
+  load.assign(static_cast<size_t>(G), 0);
+  const long long units = n * per_len;
+  for (long long i = 0; i < units; ++i) {
+    const long long k = i / G, c = i % G;
+    load[static_cast<size_t>((k & 1) ? G - 1 - c : c)] += n - i / per_len;
+  }
+  return *std::max_element(load.begin(), load.end());
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -178,9 +197,11 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
   if (L < 1 || start < 0 || kv_cap < 1) return KB_ERR_INVALID_ARG;
   if (static_cast<long long>(start) + L > kv_cap) return KB_ERR_INVALID_ARG;
   if (kv_cap > kMaxRows) return KB_ERR_UNSUPPORTED;
-  if (cta_shape != 0 && cta_shape != kb::kShapeOneTilePerSm && cta_shape != kb::kShapePersistent)
+  if (cta_shape != 0 && cta_shape != kb::kShapeOneTilePerSm && cta_shape != kb::kShapePersistent &&
+      cta_shape != kb::kShapeSnake)
     return KB_ERR_INVALID_ARG;
   const bool force_persistent = (cta_shape == kb::kShapePersistent);
+  const bool force_snake = (cta_shape == kb::kShapeSnake);
   const bool packed = (cta_shape == 0);
   if (packed && L > kb::kMaxPackedRows) return KB_ERR_INVALID_ARG;
   if (lse != nullptr && packed) return KB_ERR_INVALID_ARG;
@@ -314,7 +335,24 @@ kb_status chunk_impl(const void* q, const void* k, const void* v, void* o, int B
       const double saved = 5000.0 / (0.5 * (a.n_tiles + 1) * 1550.0 + 5000.0);
       persistent = saved > tail;
     }
-    a.persistent = (force_persistent || persistent) ? 1 : 0;
+    a.persistent = (force_persistent || persistent) ? kb::kSchedPairs : kb::kSchedOnePerCta;
+    // The snake, when it balances better than the pairs (few pairs per CTA)
+    // and all of K and V fit in three quarters of L2: it runs every group at
+    // once.
+    const long long kv_bytes = 2LL * B * Hkv * (start + L) * kb::kHeadDim * 2;
+    if (force_snake) {
+      a.persistent = kb::kSchedSnake;
+    } else if (!force_persistent && !ragged && 4 * kv_bytes <= 3 * dst->l2_bytes &&
+               pairs < 32LL * a.max_ctas) {
+      const long long n = a.n_tiles, G = a.max_ctas;
+      const long long units = n * B * Hq;
+      const long long per_cta_pairs = (pairs + G - 1) / G;
+      double est = a.persistent == kb::kSchedPairs
+                       ? per_cta_pairs * (n + 1) * 1550.0 + 5000.0
+                       : (static_cast<double>(units) * 5000.0 + 0.5 * n * (n + 1) * B * Hq * 1550.0) / G;
+      const long long snake_tiles = snake_max_tiles(n, static_cast<long long>(B) * Hq, G);
+      if (snake_tiles * 1550.0 + 5000.0 < est) a.persistent = kb::kSchedSnake;
+    }
   }
   if (ragged) {
     a.starts = ragged->starts;

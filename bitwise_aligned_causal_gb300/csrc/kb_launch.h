@@ -24,7 +24,7 @@ struct PrefillArgs {
   float* lse;              // optional [B, Hq, L] fp32: natural-log log-sum-exp of each row's scaled scores
   int seg_tiles;           // C5 segment length in key tiles (0: the whole row is one segment)
   int max_ctas;            // CTAs of a persistent launch (one per SM)
-  int persistent;          // 1: CTAs walk pairs of units; 0: one CTA per unit
+  int persistent;          // schedule: kSchedOnePerCta, kSchedPairs or kSchedSnake
   uint32_t* err;    // device error word
 };
 
@@ -62,8 +62,14 @@ constexpr int kMaxPackedRows = 32;   // query rows per (batch, head) the packed 
 // and separate Q K^T / P V issuers, so the tensor pipe works on later key
 // tiles while the softmax runs (CTA shape 3).
 constexpr int kShapeOneTilePerSm = 3;
-// The same kernel with the persistent launch forced (tests of the schedule).
+// The same kernel with the persistent launch forced (tests of the schedule):
+// 4 with pairs of query tiles, 5 with the snake.
 constexpr int kShapePersistent = 4;
+constexpr int kShapeSnake = 5;
+// The tile kernel's schedules (PrefillArgs::persistent).
+constexpr int kSchedOnePerCta = 0;   // one CTA per unit
+constexpr int kSchedPairs = 1;       // persistent, balanced pairs of query tiles, group-major
+constexpr int kSchedSnake = 2;       // persistent, single units longest first, dealt back and forth
 cudaError_t launch_prefill_s2(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const PrefillArgs& a, cudaStream_t s);
 // n_sub: 1, or 2 when the chunk crosses a 128-position tile boundary.

@@ -84,13 +84,19 @@ __device__ __forceinline__ void drain_wait2(uint32_t bar, uint32_t parity) {
 }
 
 // One work unit: (b, head, absolute query tile) and its geometry.
-// Persistent launch (one CTA per SM): units come in pairs of one head's
-// query-tile ranks r and n-1-r, whose causal lengths add up to n+1 key tiles
-// whatever r is; a CTA runs pairs blockIdx.x, blockIdx.x + gridDim.x, ...,
-// so every CTA gets the same work to within one pair.  Pairs are numbered
-// (b, kv head) slowest, so the CTAs resident at one time share one GQA
-// group's K/V in L2.  Otherwise: one unit per CTA, longest first (the
-// hardware scheduler balances), group-major or query-tile-major.
+// Persistent launch with pairs (one CTA per SM): units come in pairs of one
+// head's query-tile ranks r and n-1-r, whose causal lengths add up to n+1 key
+// tiles whatever r is; a CTA runs pairs blockIdx.x, blockIdx.x + gridDim.x,
+// ..., so every CTA gets the same work to within one pair.  Pairs are
+// numbered (b, kv head) slowest, so the CTAs resident at one time share one
+// GQA group's K/V in L2.
+// Persistent launch with a snake: single units, longest first (query-tile
+// rank slowest, then b and head), dealt to the CTAs 0..G-1 at even steps and
+// G-1..0 at odd ones, which balances to within a few key tiles when a CTA
+// gets only a few pairs' worth of work; every group's K/V is in use at once,
+// so the host takes it only when all of K and V fit in L2 with room.
+// Otherwise: one unit per CTA, longest first (the hardware scheduler
+// balances), group-major or query-tile-major.
 struct Unit {
   int b, g, h, t;       // batch, kv head, query head, absolute query tile
   int start, L;         // the sequence's first query position and row count
@@ -108,7 +114,7 @@ __device__ __forceinline__ int pairs_per_group(const PrefillArgs& args) {
 // sequence); a bad per-sequence start or length is reported and skipped.
 __device__ __forceinline__ bool unit_of(int p, int second, const PrefillArgs& args, Unit& w) {
   int tile_rank;
-  if (args.persistent) {
+  if (args.persistent == kSchedPairs) {
     const int ppg = pairs_per_group(args);
     const int bg = p / ppg;
     const int rem = p % ppg;
@@ -118,7 +124,7 @@ __device__ __forceinline__ bool unit_of(int p, int second, const PrefillArgs& ar
     w.b = bg / args.Hkv;
     w.g = bg % args.Hkv;
     w.h = w.g * kGroup + rem % kGroup;
-  } else if (args.group_major) {
+  } else if (args.persistent == kSchedOnePerCta && args.group_major) {
     const int units_per_group = args.n_tiles * kGroup;
     const int bg = p / units_per_group;
     const int rem = p % units_per_group;
@@ -156,10 +162,17 @@ __device__ __forceinline__ bool unit_of(int p, int second, const PrefillArgs& ar
   return true;
 }
 
+// The item a CTA runs at its step k: blockIdx.x + k * gridDim.x, or for the
+// snake every odd step from the other end.
+__device__ __forceinline__ int item_at(int k, const PrefillArgs& args) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return k * G + ((args.persistent == kSchedSnake && (k & 1)) ? G - 1 - c : c);
+}
+
 // Every role of a CTA walks the same units in the same order.
-#define KB_FOR_EACH_UNIT(w)                                                             \
-  for (int kb_p = blockIdx.x; kb_p < n_items; kb_p += gridDim.x)                        \
-    for (int kb_second = 0; kb_second < (args.persistent ? 2 : 1); ++kb_second)          \
+#define KB_FOR_EACH_UNIT(w)                                                                       \
+  for (int kb_k = 0, kb_p = item_at(0, args); kb_p < n_items; ++kb_k, kb_p = item_at(kb_k, args)) \
+    for (int kb_second = 0; kb_second < (args.persistent == kSchedPairs ? 2 : 1); ++kb_second)     \
       if (Unit w; unit_of(kb_p, kb_second, args, w))
 
 __global__ void __launch_bounds__(Prefill2Cfg::kThreads, 1)
@@ -176,8 +189,8 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_items = args.persistent ? args.B * args.Hkv * pairs_per_group(args)     // pairs
-                                      : args.n_tiles * args.B * args.Hq;              // units
+  const int n_items = args.persistent == kSchedPairs ? args.B * args.Hkv * pairs_per_group(args)   // pairs
+                                                     : args.n_tiles * args.B * args.Hq;            // units
   // C5 segment length in key tiles (0: the whole row is one segment)
   const int seg = args.seg_tiles > 0 ? args.seg_tiles : 0x40000000;
 
@@ -582,10 +595,12 @@ cudaError_t launch_prefill_s2(const CUtensorMap& tq, const CUtensorMap& tk, cons
     configured_device = dev;
   }
   // persistent: one CTA per SM at most, each walking its share of the unit
-  // pairs; otherwise one CTA per unit
+  // pairs or of the snake; otherwise one CTA per unit
   const long long pairs = static_cast<long long>((a.n_tiles + 1) / 2) * kGroup * a.B * a.Hkv;
-  const long long grid = a.persistent ? (pairs < a.max_ctas ? pairs : a.max_ctas)
-                                      : static_cast<long long>(a.n_tiles) * a.B * a.Hq;
+  const long long units = static_cast<long long>(a.n_tiles) * a.B * a.Hq;
+  const long long grid = a.persistent == kSchedPairs ? (pairs < a.max_ctas ? pairs : a.max_ctas)
+                         : a.persistent == kSchedSnake ? (units < a.max_ctas ? units : a.max_ctas)
+                                                       : units;
   kb_prefill_kernel_s2<<<static_cast<unsigned>(grid), Cfg::kThreads, Cfg::kSmemBytes, s>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }

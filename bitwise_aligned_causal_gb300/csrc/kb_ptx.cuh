@@ -110,6 +110,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// True while the library's error word is clear and no role of this CTA has
+// given up; otherwise sets the CTA's abort flag.  A kernel's roles call it as
+// they start, so a kernel launched after a recorded error skips its work.
+__device__ __forceinline__ bool no_error(const uint32_t* err, volatile uint32_t* abort_flag) {
+  if (*abort_flag != 0 || *reinterpret_cast<const volatile uint32_t*>(err) != 0) {
+    *abort_flag = 1;
+    return false;
+  }
+  return true;
+}
+
 // mbar_wait for a wait on the critical path that is usually short: it first
 // polls with test_wait, which never suspends the thread, so the thread goes
 // on the moment the phase completes; then it falls back to mbar_wait.

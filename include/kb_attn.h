@@ -276,8 +276,10 @@ kb_status kb_attn_backward(const void* q, const void* k, const void* v, const vo
  * q_tiles_per_cta = 3 runs the tile kernel (one 128-row query tile per CTA,
  * one CTA per SM, three score buffers, so Q K^T of later key tiles overlaps
  * the softmax of the current one), launched persistent (CTAs walk balanced
- * pairs of query tiles) or one CTA per tile as the sizes suit; 4 is 3 with
- * the persistent launch forced; 0 runs the packed kernel (the 4 heads of a
+ * pairs of query tiles, or single tiles longest first dealt to the CTAs
+ * back and forth) or one CTA per tile as the sizes suit; 4 is 3 with the
+ * persistent launch on pairs forced, 5 with the back-and-forth deal forced;
+ * 0 runs the packed kernel (the 4 heads of a
  * GQA group times the chunk's rows in one MMA tile; L <= 32).  Other values
  * return KB_ERR_INVALID_ARG.  kb_attn_chunk, kb_attn_prefill and
  * kb_attn_decode pick packed for L <= 32 and 3 otherwise.  Every shape gives

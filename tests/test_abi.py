@@ -75,7 +75,7 @@ def test_bad_sizes_rejected(kb):
     # decode context within the cache
     assert kb.kb_attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 11, 10) == kb.KB_ERR_INVALID_ARG
     assert kb.kb_attn_decode(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 0, 10) == kb.KB_ERR_INVALID_ARG
-    for shape in (1, 2, 5, -1):          # the tile kernel (3, 4) and the packed kernel (0) only
+    for shape in (1, 2, 6, -1):          # the tile kernel (3, 4, 5) and the packed kernel (0) only
         assert kb.kb_attn_chunk_cta_shape(FAKE, FAKE, FAKE, FAKE, 1, 32, 8, 4, 0, 10, shape) == kb.KB_ERR_INVALID_ARG
     assert kb.kb_attn_debug_wait_timeout(0) == kb.KB_ERR_INVALID_ARG
 

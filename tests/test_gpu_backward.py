@@ -141,3 +141,30 @@ def test_backward_bench_size_properties(kb, oracle_mod):
     rq, _, _ = oracle_mod.dq_rows(x.q, x.k, x.v, do_bits, rows)
     got = from_dev(dq)[tuple(np.asarray(rows).T)]
     assert_grad_close(got, rq, "dq rows")
+
+
+def test_backward_S8192_one_unit_elementwise(kb, oracle_mod):
+    """S=8192 with all eight KV heads in the launch: dq, dk and dv of one
+    (b, kv head) unit element by element against the oracle.  dk and dv sum
+    over the group's four query heads, so the oracle runs each head alone
+    (a group of one) and the four results are added; the four calls run in
+    threads, since ctypes releases the GIL during a foreign call."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    B, Hkv, S, g = 1, 8, 8192, 5
+    x, do_bits, dev, (dq, dk, dv, delta) = run(kb, B, Hkv, S, seed=65_000)
+    heads = range(4 * g, 4 * g + 4)
+
+    def one_head(h):
+        return oracle_mod.backward(x.q[:, h:h + 1], x.k[:, g:g + 1], x.v[:, g:g + 1], do_bits[:, h:h + 1],
+                                   n_threads=1)
+
+    with ThreadPoolExecutor(max_workers=4) as ex:
+        parts = list(ex.map(one_head, heads))
+    rk = sum(p[1] for p in parts)[0, 0]
+    rv = sum(p[2] for p in parts)[0, 0]
+    assert_grad_close(from_dev(dk)[0, g], rk, "dk")
+    assert_grad_close(from_dev(dv)[0, g], rv, "dv")
+    got_dq = from_dev(dq)[0, 4 * g:4 * g + 4]
+    for i, p in enumerate(parts):
+        assert_grad_close(got_dq[i], p[0][0, 0], f"dq head {4 * g + i}")

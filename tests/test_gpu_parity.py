@@ -116,14 +116,16 @@ def test_cache_rows_beyond_context_are_ignored(kb):
 @pytest.mark.parametrize("S", [700, 1300])
 def test_cta_shapes_give_identical_bits(kb, S):
     """The tile kernel launched one CTA per query tile or persistent (CTAs
-    walking pairs of query tiles), and short chunks on the packed kernel:
-    same contract, same bits."""
+    walking pairs of query tiles, or single tiles dealt back and forth), and
+    short chunks on the packed kernel: same contract, same bits."""
     x = inputs.make_qkv(2, S, seed=40_000 + S)
     q, k, v = to_dev(x.q), to_dev(x.k), to_dev(x.v)
     c = from_dev(kb.chunk(q, k, v, 0, q_tiles_per_cta=3))
     d = from_dev(kb.chunk(q, k, v, 0, q_tiles_per_cta=4))          # persistent launch forced
+    s = from_dev(kb.chunk(q, k, v, 0, q_tiles_per_cta=5))          # the snake schedule forced
     kb.check_device_status()
     assert np.array_equal(c, d)
+    assert np.array_equal(c, s)
     for start in (0, 130, S - 32):
         e = from_dev(kb.chunk(q[:, :, start:start + 32].contiguous(), k, v, start, q_tiles_per_cta=0))
         assert np.array_equal(e, c[:, :, start:start + 32]), start

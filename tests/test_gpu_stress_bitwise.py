@@ -128,12 +128,12 @@ def test_cta_shapes_and_packed_kernel(kb, stress):
     import torch
 
     _, q, k, v, pre = stress
-    for shape in (3, 4):
+    for shape in (3, 4, 5):
         o = kb.chunk(q, k, v, 0, q_tiles_per_cta=shape)
         assert torch.equal(o.view(torch.int16), pre.view(torch.int16)), f"CTA shape {shape}"
     for start, n in ((0, 32), (130, 20), (1000, 2), (2047, 3), (2968, 32)):
         qc = q[:, :, start:start + n].contiguous()
-        for shape in (0, 3, 4):
+        for shape in (0, 3, 4, 5):
             o = kb.chunk(qc, k, v, start, q_tiles_per_cta=shape)
             assert torch.equal(o.view(torch.int16), pre[:, :, start:start + n].view(torch.int16)), (start, n, shape)
     kb.check_device_status()
