@@ -48,14 +48,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the sources differ from that hash, the figure no longer describes the timed
 # build and the bench line reports traffic as null.
 NCU_TRAFFIC = {
-    "prefill": {"bytes": 805.80e6 + 503.86e6, "sources": "631e5448fef93f55",
+    "prefill": {"bytes": 806.05e6 + 504.00e6, "sources": "4fb3ad07fa302f54",
                 "profile": "profiles/launch_list_bench_full.md"},
-    "decode": {"bytes": 537.10e6 + 0.24e6, "sources": "2558bb14bb28d38b",
+    "decode": {"bytes": 537.09e6 + 0.24e6, "sources": "f182f6056046336c",
                "profile": "profiles/launch_list_bench_full.md"},
+    # one kb_attn_backward call: the delta, dq and dk/dv kernels together
+    "backward": {"bytes": 3797.32e6 + 775.13e6, "sources": "573c3f3ad0e67131",
+                 "profile": "profiles/launch_list_bench_full.md"},
 }
 KERNEL_SOURCES = {
     "prefill": ["kb_prefill2.cu", "kb_contract.cuh", "kb_ptx.cuh", "kb_launch.h", "kb_host.cu"],
     "decode": ["kb_decode.cu", "kb_contract.cuh", "kb_ptx.cuh", "kb_launch.h", "kb_host.cu"],
+    "backward": ["kb_backward.cu", "kb_contract.cuh", "kb_ptx.cuh", "kb_launch.h", "kb_host.cu"],
 }
 
 
@@ -540,6 +544,7 @@ def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_ma
     if bwd is not None:
         bf = 2.5 * pf                                   # dq, dk, dv: five products of the forward's size
         per_launch = bf / (bwd["bwd_ms_local"] / 1e3) / 1e12
+        tr_bwd, tr_bwd_src = traffic("backward")
         line["backward"] = {
             "value": 2.5 * aggregate(pf, world, bwd["bwd_ms"] / 1e3) / 1e12, "unit": "TFLOP/s", "ms": bwd["bwd_ms"],
             "flops": "algorithmic 2.5 x the forward's (five products over the visible pairs)",
@@ -548,7 +553,7 @@ def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_ma
                                  "ms": bwd["fwd_ms"]},
             "reps": bwd["reps"],
             "roofline": {"bound": "tensor", "achieved": per_launch, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": per_launch / peaks["bf16_tflops"], "traffic": None,
+                         "frac": per_launch / peaks["bf16_tflops"], "traffic": tr_bwd, "traffic_source": tr_bwd_src,
                          "kernel": "kb_bwd_delta_kernel + kb_bwd_dq_kernel + kb_bwd_dkdv_kernel (one call)",
                          "peak_source": peaks["source"] + " burst bf16"},
         }
