@@ -39,10 +39,13 @@
 //    its barrier; the first CTA's fold warp writes its own folded segments
 //    into the slot after them and arrives too, and warps 0-3 of that CTA
 //    (their roles are over by then) fold the slots in segment order, 16
-//    threads per row, and normalise.  When the partials do not fit there
-//    (very long contexts), each CTA keeps its own and the first one reads
-//    them through distributed shared memory after a cluster barrier.  Narrow
-//    rows only take C > 1; wide chunks run C = 1 with the folded O in TMEM.
+//    threads per row, and normalise.  When the partials do not fit there,
+//    each CTA keeps its own until the first CTA has streamed its last tile,
+//    then copies them into the first CTA's K/V rings in one bulk copy
+//    ("gather"); past the rings' size (the longest contexts) the first CTA
+//    reads them through distributed shared memory after a cluster barrier.
+//    Narrow rows only take C > 1; wide chunks run C = 1 with the folded O in
+//    TMEM.
 //  - workspace mode (the *_seg entry points): one CTA per segment writes its
 //    partial to a caller workspace, which kb_seg_fold_kernel folds.
 #include "kb_contract.cuh"
@@ -86,7 +89,8 @@ struct PackedCfg {
   static constexpr int kBarPart = kBarStEmpty + 1;         // first CTA of a cluster: every partial written
   static constexpr int kBarDrain = kBarPart + 1;           // 2: one per MMA issuer
   static constexpr int kBarQReady = kBarDrain + 2;         // Q written to shared memory by its loaders
-  static constexpr int kNumBars = kBarQReady + 1;
+  static constexpr int kBarGo = kBarQReady + 1;            // gather: the first CTA's K/V rings are free
+  static constexpr int kNumBars = kBarGo + 1;
   // Q is loaded by the softmax warps (and the fold warp when narrow) while
   // the producers' first K/V loads are already in flight
   static constexpr int kQLoaders = 32 * (kSoftmaxWarps + (kWide ? 0 : 1));
@@ -217,24 +221,35 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
   const bool zero_tail = (args.block_table != nullptr) || (args.ctx_lens != nullptr) || (args.starts != nullptr);
   const int tail_from = seq_kv - (n_kv - 1) * kTileKeys;   // first V row of the last tile past the sequence
   const uint32_t slot_bytes = static_cast<uint32_t>(n_rows) * kPartFloats * 4u;
-  // fold mode, C > 1: the other CTAs' segments (from s_first on) go to the
-  // first CTA's shared memory, followed by the first CTA's own folded
-  // segments, when they fit there ("push"); otherwise each CTA keeps its own
-  // and the first CTA reads them remotely
+  // fold mode, C > 1: the other CTAs' segments (from s_first on) reach the
+  // first CTA's shared memory in one of three ways:
+  //  - push: as each finishes, into the first CTA's partial slots, followed
+  //    by the first CTA's own folded segments, when they all fit there;
+  //  - gather: otherwise, when they fit in the first CTA's K/V rings: each
+  //    CTA keeps its partials, and once the first CTA has streamed its last
+  //    tile it lets the others copy them into its rings in one bulk copy each;
+  //  - pull: otherwise (the longest contexts), the first CTA reads them from
+  //    the others' shared memory after a cluster barrier.
   const int s_first = seg_block_start(1, ns, C);
   const bool push = C > 1 && !ws_mode &&
                     static_cast<uint32_t>(ns - s_first + 1) * slot_bytes <= static_cast<uint32_t>(Cfg::kPartBytes);
+  const bool gather = !kWide && C > 1 && !ws_mode && !push &&
+                      static_cast<uint32_t>(ns - s_first) * slot_bytes <= 2u * Cfg::kStages * kTileBytes;
+  const bool pull_sync = C > 1 && !ws_mode && !push && !gather;   // the pull path's cluster barrier
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::kNumBars; ++i) {
       uint32_t count = ((i >= Cfg::kBarPFull && i < Cfg::kBarPFull + Cfg::kSBufs) || i == Cfg::kBarORead ||
                         i == Cfg::kBarStFull || i == Cfg::kBarStEmpty)
                            ? static_cast<uint32_t>(32 * Cfg::kSoftmaxWarps) : 1u;
-      if (i == Cfg::kBarPart && C > 1) count = static_cast<uint32_t>(32 * C);   // every fold warp of the cluster
+      // push: every fold warp of the cluster; gather: the first CTA's own
+      // (the others' bytes complete its transaction count)
+      if (i == Cfg::kBarPart && C > 1) count = static_cast<uint32_t>(push ? 32 * C : 32);
       if (i == Cfg::kBarQReady) count = static_cast<uint32_t>(Cfg::kQLoaders);
       mbar_init(bar(i), count);
     }
     misc[1] = 0u;
+    if (gather && rank == 0) mbar_expect_tx(bar(Cfg::kBarPart), static_cast<uint32_t>(ns - s_first) * slot_bytes);
     fence_mbar_init();
   }
   if (warp == Cfg::kQkWarp) {
@@ -338,7 +353,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
     if (C > 1) {
       cluster_wait();
-      if (!push) cluster_sync();
+      if (pull_sync) cluster_sync();
     }
   } else if (warp == Cfg::kQkWarp) {
     // -------------------------------------------------------- Q K^T issuer
@@ -369,7 +384,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     __syncwarp();
     if (C > 1) {
       cluster_wait();
-      if (!push) cluster_sync();
+      if (pull_sync) cluster_sync();
     }
   } else if (warp == Cfg::kPvWarp) {
     // ---------------------------------------------------------- P V issuer
@@ -407,7 +422,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     __syncwarp();
     if (C > 1) {
       cluster_wait();
-      if (!push) cluster_sync();
+      if (pull_sync) cluster_sync();
     }
   } else if constexpr (kWide) {
     // ------------------------------------------------- softmax, row per thread
@@ -557,7 +572,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
     if (C > 1) {                 // wide chunks run C = 1; kept so every thread meets the same barriers
       cluster_wait();
-      if (!push) cluster_sync();
+      if (pull_sync) cluster_sync();
     }
   } else if (warp == Cfg::kFoldWarp) {
     // --------------------------------------- fold and epilogue (narrow)
@@ -667,13 +682,38 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       cluster_wait();
       // partials in shared memory are complete: the cluster's first CTA reads
       // them after this barrier
-      if (!push) cluster_sync();
+      if (pull_sync) cluster_sync();
     }
-    if (push && rank == 0) {
-      // this CTA's folded segments go to the slot after the pushed ones; warps
-      // 0-3 fold the slots once every fold warp of the cluster has arrived
+    if (gather && rank > 0) {
+      // this CTA's partials sit in its slots 0 .. n_mine-1; once the first
+      // CTA has streamed its last tile, one bulk copy moves them into its
+      // rings, at the place of their segments
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && mbar_wait_cluster(bar(Cfg::kBarGo), 0, abort_flag, args.err, kDevTimeoutSoftmax)) {
+        const int n_mine = seg_block_start(rank + 1, ns, C) - my_first;
+        bulk_copy_smem_to_cluster(
+            smem_addr_in_cta(sbase + Cfg::kKOff + static_cast<uint32_t>(my_first - s_first) * slot_bytes, 0u),
+            sbase + Cfg::kPartOff, static_cast<uint32_t>(n_mine) * slot_bytes, smem_addr_in_cta(bar(Cfg::kBarPart), 0u));
+      }
+      __syncwarp();
+    }
+    if (gather && rank == 0) {
+      // every load of this CTA has landed and been consumed (its last P V is
+      // done): the others may copy into its rings; signalled whatever
+      // happened, so no CTA waits for one that gave up
+      __syncwarp();
+      if (lane == 0)
+        for (int cr = 1; cr < C; ++cr) mbar_arrive_cluster(smem_addr_in_cta(bar(Cfg::kBarGo), static_cast<uint32_t>(cr)));
+    }
+    if ((push || gather) && rank == 0) {
+      // this CTA's folded segments go to a slot of its own (push: after the
+      // pushed ones; gather: its first partial slot, unused otherwise); warps
+      // 0-3 fold once every fold warp writing to this CTA has arrived and
+      // every copied byte has landed
       if (ok && row_used) {
-        float* slot = reinterpret_cast<float*>(smem + Cfg::kPartOff + static_cast<uint32_t>(ns - s_first) * slot_bytes);
+        float* slot = reinterpret_cast<float*>(smem + Cfg::kPartOff +
+                                               static_cast<uint32_t>(push ? ns - s_first : 0) * slot_bytes);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           *reinterpret_cast<float2*>(slot + m * 128 + 8 * q + 2 * u) =
@@ -685,7 +725,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       }
       mbar_arrive(bar(Cfg::kBarPart));                 // whatever happened, so warps 0-3 never wait for it
     }
-    if (ok && !ws_mode && rank == 0 && !push) {
+    if (ok && !ws_mode && rank == 0 && !push && !gather) {
       // fold the other CTAs' segments, in segment order, from their shared
       // memory; the next segment's partial is loaded while this one folds
       int cr = 1;                                        // rank holding the segment being loaded
@@ -721,7 +761,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
       float4 svA, svB;
       float2 ovA[16], ovB[16];
       int sgi = s_first;                                 // the first segment another CTA ran
-      const bool pull = C > 1 && !push;
+      const bool pull = pull_sync;
       if (pull && sgi < ns) load_seg(sgi, svA, ovA);
 #pragma unroll 1
       while (pull && sgi < ns) {
@@ -832,14 +872,16 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     }
     if (C > 1) {
       cluster_wait();
-      if (!push) cluster_sync();
+      if (pull_sync) cluster_sync();
     }
   }
 
-  if (push && rank == 0 && warp < 4) {
-    // ------------------------------- final fold of a push cluster (narrow)
-    // Slots 0 .. ns-s_first-1 hold segments s_first .. ns-1, the slot after
-    // them this CTA's folded segments 0 .. s_first-1.  Thread t folds packed
+  if ((push || gather) && rank == 0 && warp < 4) {
+    // ---------------------- final fold of a push or gather cluster (narrow)
+    // Slots 0 .. ns-s_first-1 (push: the partial slots; gather: the K/V
+    // rings) hold segments s_first .. ns-1; this CTA's folded segments 0 ..
+    // s_first-1 are in the partial slot after them (push) or in the first
+    // partial slot (gather).  Thread t folds packed
     // row t/16, columns 8(t%16) .. +7, left to right (C5), then C4; the
     // operations and their order are those of the fold warp's serial fold.
     const int r = threadIdx.x >> 4;
@@ -847,11 +889,13 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     bool ok = mbar_wait_cluster(bar(Cfg::kBarPart), 0, abort_flag, args.err, kDevTimeoutSoftmax);
     ok = ok && (*abort_flag == 0);
     if (ok && r < n_rows) {
-      const float* slots = reinterpret_cast<const float*>(smem + Cfg::kPartOff);
+      const float* slots = reinterpret_cast<const float*>(smem + (push ? Cfg::kPartOff : Cfg::kKOff));
+      const float* own = reinterpret_cast<const float*>(smem + Cfg::kPartOff);
       const uint32_t slot_floats = slot_bytes / 4u;
       const int n_push = ns - s_first;
       auto load = [&](int k, float4& st, float4& oa, float4& ob) {
-        const float* sl = slots + static_cast<uint32_t>(k) * slot_floats;
+        const float* sl = (k == n_push) ? (push ? slots + static_cast<uint32_t>(k) * slot_floats : own)
+                                        : slots + static_cast<uint32_t>(k) * slot_floats;
         st = *reinterpret_cast<const float4*>(sl + n_rows * 128 + 4 * r);
         oa = *reinterpret_cast<const float4*>(sl + r * 128 + 8 * cb);
         ob = *reinterpret_cast<const float4*>(sl + r * 128 + 8 * cb + 4);

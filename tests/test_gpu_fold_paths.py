@@ -6,7 +6,10 @@ of 128), runs each from the fresh softmax state and folds them left to right
 partitioned forward and decode).  The kernels fold in four places:
   - prefill and long chunks: in the softmax threads' registers;
   - a decode of a small batch: over a cluster of up to 8 CTAs, the first of
-    which folds the others' partials from their shared memory;
+    which folds the others' partials in its shared memory: pushed there as
+    they finish (up to ~15 partials), copied into its K/V rings once it has
+    streamed its last tile (B=1 ctx 32768, B=2 ctx 20000, two-row chunks),
+    or read from the others' shared memory (the longest contexts);
   - a decode of a large batch, or one whose segments exceed the cluster's
     shared-memory slots: one CTA, in registers;
   - chunks of 3-32 rows: one CTA, in TMEM;
