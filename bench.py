@@ -48,12 +48,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the sources differ from that hash, the figure no longer describes the timed
 # build and the bench line reports traffic as null.
 NCU_TRAFFIC = {
-    "prefill": {"bytes": 806.05e6 + 504.00e6, "sources": "4fb3ad07fa302f54",
+    "prefill": {"bytes": 805.69e6 + 503.41e6, "sources": "932406070fd590a4",
                 "profile": "profiles/launch_list_bench_full.md"},
-    "decode": {"bytes": 537.09e6 + 0.24e6, "sources": "f182f6056046336c",
+    "decode": {"bytes": 537.09e6 + 0.29e6, "sources": "47a2dd02a274f36c",
                "profile": "profiles/launch_list_bench_full.md"},
     # one kb_attn_backward call: the delta, dq and dk/dv kernels together
-    "backward": {"bytes": 3797.32e6 + 775.13e6, "sources": "573c3f3ad0e67131",
+    "backward": {"bytes": 3800.04e6 + 775.88e6, "sources": "8152e0344cd405e3",
                  "profile": "profiles/launch_list_bench_full.md"},
 }
 KERNEL_SOURCES = {
@@ -563,6 +563,7 @@ def emit_line(args, world, n, step_ms_max, pre_ms, dec_ms, pre_ms_max, dec_ms_ma
 
 
 GRID_PREFILL_S = (1024, 4096, 8192, 16384)
+GRID_LONG_DECODE = ((1, 16384), (1, 32768), (1, 65536), (2, 32768))
 GRID_DECODE_CTX = (128, 1024, 4096, 8192)
 GRID_B = (1, 4, 8, 16)
 
@@ -657,6 +658,19 @@ def time_grid(kb_attn, peaks, prefill_batches, device):
             out.append({"kind": "decode", "ctx": ctx, "B": B, "us": ms * 1e3, "GB/s": gbs,
                         "frac": gbs / peaks["hbm_gbs"], "copies": R, "timing": how})
             torch.cuda.empty_cache()
+    # beyond the README grid: long-context decode of small batches, where the
+    # segments of one sequence spread over a cluster and meet in one CTA
+    for B, ctx in GRID_LONG_DECODE:
+        gen.manual_seed(9_500_000 + ctx + B)
+        per_copy = decode_bytes(B, ctx)
+        ms, R, how = rotating_launch_ms(
+            lambda: (randn((B, HQ, 1, D)), randn((B, HKV, ctx, D)), randn((B, HKV, ctx, D)),
+                     torch.empty((B, HQ, 1, D), device=device, dtype=torch.bfloat16)),
+            lambda t: kb_attn.decode(t[0], t[1], t[2], ctx, out=t[3]), per_copy, device, min_launches=24)
+        gbs = decode_bytes(B, ctx) / (ms / 1e3) / 1e9
+        out.append({"kind": "decode_long", "ctx": ctx, "B": B, "us": ms * 1e3, "GB/s": gbs,
+                    "frac": gbs / peaks["hbm_gbs"], "copies": R, "timing": how})
+        torch.cuda.empty_cache()
     kb_attn.check_device_status()
     return out
 
@@ -666,6 +680,7 @@ def grid_summary(records, peaks):
     decode bar over all 16 (B, ctx) cells, here as mean fractions of roofline."""
     pre = [r for r in records if r["kind"] == "prefill" and r["B"] == 1]
     dec = [r for r in records if r["kind"] == "decode"]
+    long_ctx = [r for r in records if r["kind"] == "decode_long"]
     return {
         "workload": ("KernelBraid README grid: prefill B=1, S in 1K/4K/8K/16K; decode B in 1/4/8/16 x ctx in 128/1K/4K/8K; "
                      "Hq=32 Hkv=8 D=128 bf16, torch.randn inputs; each configuration timed over back-to-back "
@@ -677,6 +692,8 @@ def grid_summary(records, peaks):
                                                 "frac": round(r["frac"], 4)} for r in dec},
         "prefill_bar_mean_frac": statistics.mean(r["frac"] for r in pre),
         "decode_bar_mean_frac": statistics.mean(r["frac"] for r in dec),
+        "decode_long_ctx": {f"B{r['B']}_ctx{r['ctx']}": {"GB/s": round(r["GB/s"], 1), "us": round(r["us"], 2),
+                                                        "frac": round(r["frac"], 4)} for r in long_ctx},
         "peaks": {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "source": peaks["source"]},
     }
 

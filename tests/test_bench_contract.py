@@ -89,9 +89,12 @@ def test_grid_summary_reports_both_bars():
             for S in bench.GRID_PREFILL_S]
     recs += [{"kind": "decode", "ctx": c, "B": b, "us": 10.0, "GB/s": 4000.0, "frac": 0.5, "timing": "graph"}
              for c in bench.GRID_DECODE_CTX for b in bench.GRID_B]
+    recs += [{"kind": "decode_long", "ctx": c, "B": b, "us": 30.0, "GB/s": 6000.0, "frac": 0.9, "timing": "graph"}
+             for b, c in bench.GRID_LONG_DECODE]
     g = bench.grid_summary(recs, peaks)
     assert len(g["prefill_b1"]) == 4 and len(g["decode"]) == 16
     assert g["prefill_bar_mean_frac"] == pytest.approx(0.5) and g["decode_bar_mean_frac"] == pytest.approx(0.5)
+    assert len(g["decode_long_ctx"]) == len(bench.GRID_LONG_DECODE)      # reported, outside the README's bar
     d = _emit(grid=g)
     assert d["grid"]["decode"]["B1_ctx8192"]["frac"] == 0.5
 
