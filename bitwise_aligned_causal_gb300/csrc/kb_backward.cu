@@ -131,13 +131,19 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // (b, h, query tile t), longest first; group-major beyond a few waves
+  // (b, h, query tile t), longest first; beyond a few waves group-major in
+  // windows of two groups (the longest tiles of both groups first)
   int b, g, h, tile_rank;
   if (args.group_major) {
-    const int per_group = args.n_tiles * kGroup;
-    const int bg = blockIdx.x / per_group;
-    const int rem = blockIdx.x % per_group;
-    tile_rank = rem / kGroup;
+    constexpr int kWin = 2;
+    const int BG = args.B * args.Hkv, per = args.n_tiles * kGroup, full = BG / kWin;
+    const int bid = static_cast<int>(blockIdx.x);
+    int w, r, wg;
+    if (bid < full * kWin * per) { w = bid / (kWin * per); r = bid % (kWin * per); wg = kWin; }
+    else { w = full; r = bid - full * kWin * per; wg = BG - full * kWin; }
+    tile_rank = r / (wg * kGroup);
+    const int rem = r % (wg * kGroup);
+    const int bg = w * kWin + rem / kGroup;
     b = bg / args.Hkv;
     g = bg % args.Hkv;
     h = g * kGroup + rem % kGroup;
@@ -394,10 +400,21 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // (b, kv head g, key tile jt): (b, g) slowest so resident CTAs share the
-  // group's q and dO in L2; within a group the longest (jt = 0) first
-  const int bg = blockIdx.x / args.n_tiles;
-  const int jt = blockIdx.x % args.n_tiles;
+  // (b, kv head g, key tile jt) in windows of two groups, (b, g) windows
+  // slowest so resident CTAs share the groups' q and dO in L2; within a
+  // window the longest key tiles (jt = 0) of both groups first, so the last
+  // window's longest CTAs start early and the launch ends on short ones
+  int bg, jt;
+  {
+    constexpr int kWin = 2;
+    const int BG = args.B * args.Hkv, n = args.n_tiles, full = BG / kWin;
+    const int bid = static_cast<int>(blockIdx.x);
+    int w, r, wg;
+    if (bid < full * kWin * n) { w = bid / (kWin * n); r = bid % (kWin * n); wg = kWin; }
+    else { w = full; r = bid - full * kWin * n; wg = BG - full * kWin; }
+    jt = r / wg;
+    bg = w * kWin + r % wg;
+  }
   const int b = bg / args.Hkv;
   const int g = bg % args.Hkv;
   const int n_q = args.n_tiles - jt;                  // query tiles jt..n-1 see this key tile

@@ -152,6 +152,32 @@ def test_paged_decode_bad_device_arguments_are_reported(kb):
     assert kb.kb_attn_check_device_status(None) == kb.KB_OK
 
 
+def test_paged_decode_long_contexts_over_a_cluster(kb):
+    """B=2 with 20000 and 9000 keys: the segments of each sequence spread over a
+    cluster whose partials overflow the first CTA's slots (they are gathered into
+    its K/V rings); bits equal the contiguous decode of each sequence alone.  A
+    context length beyond the pool is then reported, and the next call is clean."""
+    import torch
+
+    B, S = 2, 20000
+    x = inputs.make_qkv(B, S, seed=75_000, Lq=1)
+    k, v = to_dev(x.k), to_dev(x.v)
+    qd = to_dev(x.q)
+    ctx = np.array([20000, 9000], dtype=np.int32)
+    kp, vp, table = _paged(k, v, ctx, 128, seed=75_001)
+    out = from_dev(kb.decode_paged(qd, kp, vp, table, torch.tensor(ctx, device="cuda")))
+    kb.check_device_status()
+    for b in range(B):
+        cont = from_dev(kb.decode(qd[b:b + 1], k[b:b + 1], v[b:b + 1], int(ctx[b])))
+        assert np.array_equal(out[b:b + 1], cont), f"batch {b}"
+    bad = torch.tensor([20000, 30000], dtype=torch.int32, device="cuda")      # beyond the pages of sequence 1
+    kb.decode_paged(qd, kp, vp, table, bad)
+    assert kb.kb_attn_check_device_status(None) == kb.KB_ERR_INVALID_ARG
+    again = from_dev(kb.decode_paged(qd, kp, vp, table, torch.tensor(ctx, device="cuda")))
+    assert kb.kb_attn_check_device_status(None) == kb.KB_OK
+    assert np.array_equal(again, out)
+
+
 @pytest.mark.parametrize("page_size", [128, 384])
 @pytest.mark.parametrize("start,L", [(0, 1100), (0, 33), (200, 300), (1000, 100), (1099, 1), (64, 32), (500, 17)])
 def test_paged_chunks_bitwise_equal_prefill(kb, seq, page_size, start, L):
