@@ -62,8 +62,9 @@ def test_decode_equals_prefill_and_workspace_fold(kb, oracle_mod, B, ctx):
 
 @pytest.mark.parametrize("ctx", [122_880, 131_072])
 def test_very_long_decode(kb, oracle_mod, ctx):
-    """120 segments fill a cluster of 8 CTAs' shared-memory slots exactly; 128
-    segments do not, and the decode folds them all in one CTA instead."""
+    """120 segments fill a cluster of 8 CTAs' shared-memory slots exactly (too
+    many for the first CTA's rings, so it reads them remotely); 128 segments do
+    not, and the decode folds them all in one CTA instead."""
     x = inputs.make_qkv(1, ctx, seed=111_000 + ctx, Lq=1)
     q, k, v = to_dev(x.q), to_dev(x.k), to_dev(x.v)
     dec = from_dev(kb.decode(q, k, v, ctx))

@@ -16,10 +16,11 @@ supported workloads):
     3-32 rows (packed kernel, wide) and 33-400 rows (tile kernel, start != 0);
   - decodes at positions around key-tile boundaries;
   - paged chunks, paged decode and a ragged batch;
-  - the tile kernel's two launches (CTA shapes 3 and 4) and the packed kernel;
-  - the segmented mode: prefill_seg = chunk_seg = decode_seg.
-Sampled rows of the default and the segmented prefill are checked against
-the fp64 oracle.
+  - the tile kernel's launches (CTA shapes 3, 4 and 5: by size, persistent
+    pairs, persistent snake) and the packed kernel;
+  - explicit segment lengths: prefill_seg = chunk_seg = decode_seg.
+Sampled rows of the default and the explicit-length prefill are checked
+against the fp64 oracle.
 """
 
 import numpy as np
