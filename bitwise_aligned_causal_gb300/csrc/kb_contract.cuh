@@ -205,10 +205,16 @@ __device__ __forceinline__ float row_softmax_tile_quad(float (&x)[32], int u, in
       x[2 * r + 1] = (8 * r + 2 * u + 1 < n_valid) ? x[2 * r + 1] : -INFINITY;
     }
   }
-  float mx[8];
+  // exact maximum (order-free): 32 values in 16 three- and two-input maxima
+  float mx[12];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) mx[i] = max3(x[i], x[i + 8], fmaxf(x[i + 16], x[i + 24]));
-  float tile_max = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+  for (int i = 0; i < 10; ++i) mx[i] = max3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  mx[10] = x[30];
+  mx[11] = x[31];
+  float my[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) my[i] = max3(mx[3 * i], mx[3 * i + 1], mx[3 * i + 2]);
+  float tile_max = fmaxf(max3(my[0], my[1], my[2]), my[3]);
   tile_max = fmaxf(tile_max, __shfl_xor_sync(0xffffffffu, tile_max, 1));
   tile_max = fmaxf(tile_max, __shfl_xor_sync(0xffffffffu, tile_max, 2));
 
