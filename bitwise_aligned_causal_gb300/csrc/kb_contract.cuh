@@ -142,18 +142,23 @@ __device__ __forceinline__ float row_softmax_tile(const uint32_t (&s)[128], int 
     if (kMasked) x[k] = (k < n_valid) ? x[k] : -INFINITY;
   }
 
-  // exact row max (max is order-free): 16 lanes of three-input maxima
-  float mx[16];
+  // exact row max (max is order-free): 128 values in 64 three- and two-input
+  // maxima, five levels deep
+  float m1[44];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    mx[i] = max3(x[i], x[i + 16], x[i + 32]);
-    mx[i] = max3(mx[i], x[i + 48], x[i + 64]);
-    mx[i] = max3(mx[i], x[i + 80], x[i + 96]);
-    mx[i] = fmaxf(mx[i], x[i + 112]);
-  }
+  for (int i = 0; i < 42; ++i) m1[i] = max3(x[3 * i], x[3 * i + 1], x[3 * i + 2]);
+  m1[42] = x[126];
+  m1[43] = x[127];
+  float m2[16];
 #pragma unroll
-  for (int i = 0; i < 5; ++i) mx[i] = max3(mx[i], mx[i + 5], mx[i + 10]);
-  const float tile_max = max3(max3(mx[0], mx[1], mx[2]), mx[3], fmaxf(mx[4], mx[15]));
+  for (int i = 0; i < 14; ++i) m2[i] = max3(m1[3 * i], m1[3 * i + 1], m1[3 * i + 2]);
+  m2[14] = m1[42];
+  m2[15] = m1[43];
+  float m3[6];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) m3[i] = max3(m2[3 * i], m2[3 * i + 1], m2[3 * i + 2]);
+  m3[5] = m2[15];
+  const float tile_max = fmaxf(max3(m3[0], m3[1], m3[2]), max3(m3[3], m3[4], m3[5]));
 
   float alpha = 1.0f;
   if (__fsub_rn(tile_max, st.m) > kRescaleThresholdRaw) {
