@@ -48,12 +48,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the sources differ from that hash, the figure no longer describes the timed
 # build and the bench line reports traffic as null.
 NCU_TRAFFIC = {
-    "prefill": {"bytes": 805.94e6 + 503.86e6, "sources": "55afb43d8738fbe1",
+    "prefill": {"bytes": 806.14e6 + 503.91e6, "sources": "425d0754c4dad496",
                 "profile": "profiles/launch_list_bench_full.md"},
-    "decode": {"bytes": 537.12e6 + 0.30e6, "sources": "1115b8f4fd1c3234",
+    "decode": {"bytes": 537.09e6 + 0.26e6, "sources": "4441b300c14652c7",
                "profile": "profiles/launch_list_bench_full.md"},
     # one kb_attn_backward call: the delta, dq and dk/dv kernels together
-    "backward": {"bytes": 3831.70e6 + 774.31e6, "sources": "107aa433f63cd3f2",
+    "backward": {"bytes": 3832.40e6 + 773.93e6, "sources": "0f8f0ce2cdfc9fce",
                  "profile": "profiles/launch_list_bench_full.md"},
 }
 KERNEL_SOURCES = {
