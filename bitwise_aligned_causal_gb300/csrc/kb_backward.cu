@@ -91,22 +91,28 @@ __global__ void __launch_bounds__(256) kb_bwd_delta_kernel(const __nv_bfloat16* 
 // -------------------------------------------------------------- dq kernel
 
 struct BwdQCfg {
-  static constexpr int kThreads = 352;        // 8 elementwise warps, producer, two MMA issuers
-  static constexpr int kLoadWarp = 8;
+  static constexpr int kThreads = 384;        // 8 elementwise warps, two producers, two MMA issuers
+  static constexpr int kLoadWarp = 8;         // Q, dO and the K ring
   static constexpr int kMmaWarp = 9;          // TMEM allocator + S, dP issuer
   static constexpr int kDqWarp = 10;          // dQ issuer
-  static constexpr int kStages = 2;           // K/V ring
+  static constexpr int kLoadWarpV = 11;       // the V ring
+  // K(j) is read by S(j) and by dQ(j), V(j) only by dP(j): the K ring frees
+  // a slot after dQ(j), the V ring after S(j), dP(j), so V needs fewer slots
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 2;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDS = 384;
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kDOOff = kTileBytes;
   static constexpr uint32_t kKOff = 2 * kTileBytes;
-  static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
-  static constexpr uint32_t kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr uint32_t kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr uint32_t kBarOff = kVOff + kVStages * kTileBytes;
   static constexpr int kBarQD = 0;                         // Q and dO landed
-  static constexpr int kBarKVFull = 1;                     // 2: K(j), V(j) landed in slot j%2
-  static constexpr int kBarKVEmpty = kBarKVFull + kStages; // 2: dQ(j) done, slot j%2 free
-  static constexpr int kBarSFull = kBarKVEmpty + kStages;  // S(j), dP(j) in TMEM
+  static constexpr int kBarKFull = 1;                      // 3: K(j) landed in slot j%3
+  static constexpr int kBarKEmpty = kBarKFull + kKStages;  // 3: dQ(j) done, K slot j%3 free
+  static constexpr int kBarVFull = kBarKEmpty + kKStages;  // 2: V(j) landed in slot j%2
+  static constexpr int kBarVEmpty = kBarVFull + kVStages;  // 2: S(j), dP(j) done, V slot j%2 free
+  static constexpr int kBarSFull = kBarVEmpty + kVStages;  // S(j), dP(j) in TMEM
   static constexpr int kBarSFree = kBarSFull + 1;          // S(j), dP(j) read (256 arrivals)
   static constexpr int kBarDSFull = kBarSFree + 1;         // dS(j) in TMEM (256 arrivals)
   static constexpr int kBarDQDone = kBarDSFull + 1;        // dQ += dS(j) K(j) finished
@@ -173,41 +179,45 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   const uint32_t tmem_base = misc[0];
   const bool skip = (*abort_flag != 0);
 
-  if (warp == Cfg::kLoadWarp) {
-    // ------------------------------------------------------------ producer
+  if (warp == Cfg::kLoadWarp || warp == Cfg::kLoadWarpV) {
+    // ----------------------------------------------------------- producers
+    // One warp per ring: Q, dO and K; V.
+    const bool is_v = (warp == Cfg::kLoadWarpV);
     if (!skip) {
       const uint64_t keep = l2_policy_evict_last();
+      const int stages = is_v ? Cfg::kVStages : Cfg::kKStages;
+      const int full0 = is_v ? Cfg::kBarVFull : Cfg::kBarKFull;
+      const int empty0 = is_v ? Cfg::kBarVEmpty : Cfg::kBarKEmpty;
+      const uint32_t ring = sbase + (is_v ? Cfg::kVOff : Cfg::kKOff);
+      const CUtensorMap* tmap = is_v ? &tmap_v : &tmap_k;
       if (lane == 0) {
-        tma_prefetch_desc(&tmap_q);
-        tma_prefetch_desc(&tmap_do);
-        tma_prefetch_desc(&tmap_k);
-        tma_prefetch_desc(&tmap_v);
-        mbar_arrive_expect_tx(bar(Cfg::kBarQD), 2 * kTileBytes);
-        tma_load_tile(sbase + Cfg::kQOff, &tmap_q, t * kTileRows, b * args.Hq + h, bar(Cfg::kBarQD));
-        tma_load_tile(sbase + Cfg::kDOOff, &tmap_do, t * kTileRows, b * args.Hq + h, bar(Cfg::kBarQD));
+        tma_prefetch_desc(tmap);
+        if (!is_v) {
+          tma_prefetch_desc(&tmap_q);
+          tma_prefetch_desc(&tmap_do);
+          mbar_arrive_expect_tx(bar(Cfg::kBarQD), 2 * kTileBytes);
+          tma_load_tile(sbase + Cfg::kQOff, &tmap_q, t * kTileRows, b * args.Hq + h, bar(Cfg::kBarQD));
+          tma_load_tile(sbase + Cfg::kDOOff, &tmap_do, t * kTileRows, b * args.Hq + h, bar(Cfg::kBarQD));
+        }
       }
       int issued = 0;
       bool ok = true;
       for (int j = 0; j < n_kv; ++j) {
-        const int slot = j % Cfg::kStages;
-        if (j >= Cfg::kStages)
-          ok = mbar_wait(bar(Cfg::kBarKVEmpty + slot), ((j / Cfg::kStages) - 1) & 1, abort_flag, args.err,
-                         kDevTimeoutSlot);
+        const int slot = j % stages;
+        if (j >= stages)
+          ok = mbar_wait(bar(empty0 + slot), ((j / stages) - 1) & 1, abort_flag, args.err, kDevTimeoutSlot);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar(Cfg::kBarKVFull + slot), 2 * kTileBytes);
-          tma_load_tile_hint(sbase + Cfg::kKOff + slot * kTileBytes, &tmap_k, j * kTileRows, b * args.Hkv + g,
-                             bar(Cfg::kBarKVFull + slot), keep);
-          tma_load_tile_hint(sbase + Cfg::kVOff + slot * kTileBytes, &tmap_v, j * kTileRows, b * args.Hkv + g,
-                             bar(Cfg::kBarKVFull + slot), keep);
+          mbar_arrive_expect_tx(bar(full0 + slot), kTileBytes);
+          tma_load_tile_hint(ring + slot * kTileBytes, tmap, j * kTileRows, b * args.Hkv + g, bar(full0 + slot), keep);
         }
         issued = j + 1;
       }
       if (!ok && lane == 0) {
-        drain_wait_b(bar(Cfg::kBarQD), 0);
-        for (int x = (issued > Cfg::kStages ? issued - Cfg::kStages : 0); x < issued; ++x)
-          drain_wait_b(bar(Cfg::kBarKVFull + x % Cfg::kStages), (x / Cfg::kStages) & 1);
+        if (!is_v) drain_wait_b(bar(Cfg::kBarQD), 0);
+        for (int x = (issued > stages ? issued - stages : 0); x < issued; ++x)
+          drain_wait_b(bar(full0 + x % stages), (x / stages) & 1);
       }
     }
   } else if (warp == Cfg::kMmaWarp) {
@@ -219,14 +229,16 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       const uint32_t q_s = sbase + Cfg::kQOff, do_s = sbase + Cfg::kDOOff;
       bool ok = mbar_wait(bar(Cfg::kBarQD), 0, abort_flag, args.err, kDevTimeoutTma);
       for (int j = 0; j < n_kv && ok; ++j) {
-        const int slot = j % Cfg::kStages;
-        ok = mbar_wait(bar(Cfg::kBarKVFull + slot), (j / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+        const int ks = j % Cfg::kKStages, vs = j % Cfg::kVStages;
+        ok = mbar_wait(bar(Cfg::kBarKFull + ks), (j / Cfg::kKStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+        if (ok) ok = mbar_wait(bar(Cfg::kBarVFull + vs), (j / Cfg::kVStages) & 1, abort_flag, args.err, kDevTimeoutTma);
         if (ok && j > 0) ok = mbar_wait(bar(Cfg::kBarSFree), (j - 1) & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
-        issue_qk_pair(tmem_base + Cfg::kColS, q_s, sbase + Cfg::kKOff + slot * kTileBytes,
-                      tmem_base + Cfg::kColDP, do_s, sbase + Cfg::kVOff + slot * kTileBytes);
+        issue_qk_pair(tmem_base + Cfg::kColS, q_s, sbase + Cfg::kKOff + ks * kTileBytes,
+                      tmem_base + Cfg::kColDP, do_s, sbase + Cfg::kVOff + vs * kTileBytes);
         tc_commit(bar(Cfg::kBarSFull));
+        tc_commit(bar(Cfg::kBarVEmpty + vs));
       }
       if (!ok) {
         tc_commit(bar(Cfg::kBarDrain));
@@ -235,18 +247,18 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     }
   } else if (warp == Cfg::kDqWarp) {
     // ---------------------------------------------------------- dQ issuer
-    // dQ(j) reads dS(j) and K(j); the K/V slot is released after it (S(j) and
-    // dP(j) finished before dS(j) existed).
+    // dQ(j) reads dS(j) and K(j); the K slot is released after it (S(j)
+    // finished before dS(j) existed).
     if (lane == 0 && !skip) {
       bool ok = true;
       for (int j = 0; j < n_kv && ok; ++j) {
         ok = mbar_wait(bar(Cfg::kBarDSFull), j & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
-        const int slot = j % Cfg::kStages;
-        issue_pv(tmem_base + Cfg::kColDQ, tmem_base + Cfg::kColDS, sbase + Cfg::kKOff + slot * kTileBytes, j == 0);
+        const int ks = j % Cfg::kKStages;
+        issue_pv(tmem_base + Cfg::kColDQ, tmem_base + Cfg::kColDS, sbase + Cfg::kKOff + ks * kTileBytes, j == 0);
         tc_commit(bar(Cfg::kBarDQDone));
-        tc_commit(bar(Cfg::kBarKVEmpty + slot));
+        tc_commit(bar(Cfg::kBarKEmpty + ks));
       }
       if (!ok) {
         tc_commit(bar(Cfg::kBarDrain + 1));
