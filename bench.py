@@ -53,7 +53,7 @@ NCU_TRAFFIC = {
     "decode": {"bytes": 537.09e6 + 0.26e6, "sources": "4441b300c14652c7",
                "profile": "profiles/launch_list_bench_full.md"},
     # one kb_attn_backward call: the delta, dq and dk/dv kernels together
-    "backward": {"bytes": 3832.40e6 + 773.93e6, "sources": "0f8f0ce2cdfc9fce",
+    "backward": {"bytes": 3831.32e6 + 774.20e6, "sources": "06e85b366bf3a526",
                  "profile": "profiles/launch_list_bench_full.md"},
 }
 KERNEL_SOURCES = {
