@@ -406,7 +406,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         if (ok && first && F > 0)
           ok = mbar_wait(bar(Cfg::kBarORead), (F - 1) & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (ok)
-          ok = mbar_wait(bar(Cfg::kBarPFull + sb), (j / Cfg::kSBufs) & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+          ok = mbar_wait_hint(bar(Cfg::kBarPFull + sb), (j / Cfg::kSBufs) & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
         issue_pv(tmem_base + Cfg::kOCol, tmem_base + sb * 128u, sbase + Cfg::kVOff + slot * kTileBytes, first);
@@ -438,7 +438,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     int js = 0;                                        // tile index within its segment (j0 starts one)
     bool ok = run && no_error(args.err, abort_flag);
     for (int j = 0; j < nt && ok; ++j) {               // j: tile j0 + j
-      ok = mbar_wait(bar(Cfg::kBarSFull + j % Cfg::kSBufs), (j / Cfg::kSBufs) & 1, abort_flag, args.err,
+      ok = mbar_wait_hint(bar(Cfg::kBarSFull + j % Cfg::kSBufs), (j / Cfg::kSBufs) & 1, abort_flag, args.err,
                      kDevTimeoutMma);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -805,7 +805,7 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
     int G = 0;                                         // segments handed to the fold warp
     bool ok = run && no_error(args.err, abort_flag);
     for (int j = 0; j < nt && ok; ++j) {                    // j: tile j0 + j
-      ok = mbar_wait(bar(Cfg::kBarSFull + j % Cfg::kSBufs), (j / Cfg::kSBufs) & 1, abort_flag, args.err,
+      ok = mbar_wait_hint(bar(Cfg::kBarSFull + j % Cfg::kSBufs), (j / Cfg::kSBufs) & 1, abort_flag, args.err,
                      kDevTimeoutMma);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
