@@ -48,12 +48,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the sources differ from that hash, the figure no longer describes the timed
 # build and the bench line reports traffic as null.
 NCU_TRAFFIC = {
-    "prefill": {"bytes": 806.14e6 + 503.91e6, "sources": "425d0754c4dad496",
+    "prefill": {"bytes": 806.23e6 + 503.38e6, "sources": "fc78aae055077c17",
                 "profile": "profiles/launch_list_bench_full.md"},
-    "decode": {"bytes": 537.09e6 + 0.26e6, "sources": "4441b300c14652c7",
+    "decode": {"bytes": 537.09e6 + 0.45e6, "sources": "9a0cb83ce5b66799",
                "profile": "profiles/launch_list_bench_full.md"},
     # one kb_attn_backward call: the delta, dq and dk/dv kernels together
-    "backward": {"bytes": 3831.32e6 + 774.20e6, "sources": "06e85b366bf3a526",
+    "backward": {"bytes": 3833.50e6 + 774.21e6, "sources": "dc0c8e30b6b79921",
                  "profile": "profiles/launch_list_bench_full.md"},
 }
 KERNEL_SOURCES = {
