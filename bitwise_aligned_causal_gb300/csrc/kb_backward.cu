@@ -230,8 +230,8 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       bool ok = mbar_wait(bar(Cfg::kBarQD), 0, abort_flag, args.err, kDevTimeoutTma);
       for (int j = 0; j < n_kv && ok; ++j) {
         const int ks = j % Cfg::kKStages, vs = j % Cfg::kVStages;
-        ok = mbar_wait(bar(Cfg::kBarKFull + ks), (j / Cfg::kKStages) & 1, abort_flag, args.err, kDevTimeoutTma);
-        if (ok) ok = mbar_wait(bar(Cfg::kBarVFull + vs), (j / Cfg::kVStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+        ok = mbar_wait_hint(bar(Cfg::kBarKFull + ks), (j / Cfg::kKStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+        if (ok) ok = mbar_wait_hint(bar(Cfg::kBarVFull + vs), (j / Cfg::kVStages) & 1, abort_flag, args.err, kDevTimeoutTma);
         if (ok && j > 0) ok = mbar_wait_hint(bar(Cfg::kBarSFree), (j - 1) & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
@@ -518,7 +518,7 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         const int slot = s % Cfg::kStages;
         const uint32_t q_s = sbase + Cfg::kQOff + slot * Cfg::kSlotBytes;
         const uint32_t do_s = q_s + kTileBytes;
-        ok = mbar_wait(bar(Cfg::kBarQDFull + slot), (s / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
+        ok = mbar_wait_hint(bar(Cfg::kBarQDFull + slot), (s / Cfg::kStages) & 1, abort_flag, args.err, kDevTimeoutTma);
         if (!ok) break;
         tc_fence_after();
         issue_qk_pair(tmem_base + Cfg::kColST, sbase + Cfg::kKOff, q_s, tmem_base + Cfg::kColDPT, sbase + Cfg::kVOff,
@@ -556,7 +556,7 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       const int slot = s % Cfg::kStages;
       const bool diag = (s % n_q) == 0;                              // query tile jt: keys past the row masked
       ok = mbar_wait_hint(bar(Cfg::kBarSTFull), s & 1, abort_flag, args.err, kDevTimeoutMma);
-      if (ok) ok = mbar_wait(bar(Cfg::kBarVecFull + slot), (s / Cfg::kStages) & 1, abort_flag, args.err,
+      if (ok) ok = mbar_wait_hint(bar(Cfg::kBarVecFull + slot), (s / Cfg::kStages) & 1, abort_flag, args.err,
                              kDevTimeoutTma);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
