@@ -53,7 +53,7 @@ NCU_TRAFFIC = {
     "decode": {"bytes": 537.09e6 + 0.45e6, "sources": "9a0cb83ce5b66799",
                "profile": "profiles/launch_list_bench_full.md"},
     # one kb_attn_backward call: the delta, dq and dk/dv kernels together
-    "backward": {"bytes": 3833.50e6 + 774.21e6, "sources": "dc0c8e30b6b79921",
+    "backward": {"bytes": 3830.31e6 + 773.74e6, "sources": "f4db4f5479dd4cf2",
                  "profile": "profiles/launch_list_bench_full.md"},
 }
 KERNEL_SOURCES = {
