@@ -63,6 +63,31 @@ __device__ __forceinline__ void issue_pv_pair(uint32_t d1, uint32_t a1_tmem, uin
   }
 }
 
+// 16x256b loads of 32 columns (four repetitions) from two addresses, one
+// wait: thread t gets lanes t/4 and t/4 + 8, columns 8r + 2(t%4) and
+// 8r + 2(t%4) + 1 of repetition r in registers 4r, 4r+1 (first lane) and
+// 4r+2, 4r+3 (second lane).
+__device__ __forceinline__ void tmem_ld_16x256b_x4_pair_wait(uint32_t ta, uint32_t tb, uint32_t (&ra)[16],
+                                                             uint32_t (&rb)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(ra[0]), "=r"(ra[1]), "=r"(ra[2]), "=r"(ra[3]), "=r"(ra[4]), "=r"(ra[5]), "=r"(ra[6]), "=r"(ra[7]),
+        "=r"(ra[8]), "=r"(ra[9]), "=r"(ra[10]), "=r"(ra[11]), "=r"(ra[12]), "=r"(ra[13]), "=r"(ra[14]), "=r"(ra[15]),
+        "=r"(rb[0]), "=r"(rb[1]), "=r"(rb[2]), "=r"(rb[3]), "=r"(rb[4]), "=r"(rb[5]), "=r"(rb[6]), "=r"(rb[7]),
+        "=r"(rb[8]), "=r"(rb[9]), "=r"(rb[10]), "=r"(rb[11]), "=r"(rb[12]), "=r"(rb[13]), "=r"(rb[14]), "=r"(rb[15])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+// 16x128b store of 16 columns (four repetitions): thread t writes lanes t/4
+// and t/4 + 8, column 4r + t%4 of repetition r, from registers 2r and 2r+1.
+__device__ __forceinline__ void tmem_st_16x128b_x4(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+               ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -388,9 +413,9 @@ struct BwdKVCfg {
   static constexpr int kBarQDEmpty = kBarQDFull + kStages;            // 2: dV, dK of step s done
   static constexpr int kBarVecFull = kBarQDEmpty + kStages;           // 2: lse2, delta of step s (32 arrivals)
   static constexpr int kBarSTFull = kBarVecFull + kStages;            // S^T, dP^T of step s in TMEM
-  static constexpr int kBarPDSFull = kBarSTFull + 1;                  // 2: P^T, dS^T of query half 0 / 1
+  static constexpr int kBarPDSFull = kBarSTFull + 1;                  // 4: P^T, dS^T of query quarter 0..3
                                                                       //    stored (256 arrivals each)
-  static constexpr int kBarDone = kBarPDSFull + 2;                    // every dV, dK product finished
+  static constexpr int kBarDone = kBarPDSFull + 4;                    // every dV, dK product finished
   static constexpr int kBarDrain = kBarDone + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
@@ -435,7 +460,7 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::kNumBars; ++i) {
       uint32_t count = 1u;
-      if (i == Cfg::kBarPDSFull || i == Cfg::kBarPDSFull + 1) count = 256u;
+      if (i >= Cfg::kBarPDSFull && i < Cfg::kBarPDSFull + 4) count = 256u;
       if (i >= Cfg::kBarVecFull && i < Cfg::kBarVecFull + Cfg::kStages) count = 32u;
       mbar_init(bar(i), count);
     }
@@ -506,12 +531,12 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     }
   } else if (warp == Cfg::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    // per step: S^T = K Q^T, dP^T = V dO^T | (P^T, dS^T of queries 0-63
-    // stored) K steps 0-3 of dV += P^T dO, dK += dS^T Q | (queries 64-127)
-    // K steps 4-7.  The first four steps read only the columns the first
-    // half wrote, so they run while the second half is computed.  P^T and
-    // dS^T overwrite S^T and dP^T, whose next values are issued after these
-    // products (in issue order).
+    // per step: S^T = K Q^T, dP^T = V dO^T, then for each quarter of the
+    // query columns (32 queries), once its P^T and dS^T are stored, K steps
+    // 2q and 2q+1 of dV += P^T dO and dK += dS^T Q.  A quarter's steps read
+    // only the columns that quarter wrote, so they run while the next quarter
+    // is computed.  P^T and dS^T overwrite S^T and dP^T, whose next values are
+    // issued after these products (in issue order).
     if (lane == 0 && !skip) {
       bool ok = mbar_wait(bar(Cfg::kBarKV), 0, abort_flag, args.err, kDevTimeoutTma);
       for (int s = 0; s < n_steps && ok; ++s) {
@@ -527,12 +552,22 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         ok = mbar_wait_hint(bar(Cfg::kBarPDSFull), s & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
-        issue_pv_pair<0, 4>(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, tmem_base + Cfg::kColDK,
+        issue_pv_pair<0, 2>(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, tmem_base + Cfg::kColDK,
                             tmem_base + Cfg::kColDPT, q_s, s == 0);
         ok = mbar_wait_hint(bar(Cfg::kBarPDSFull + 1), s & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
-        issue_pv_pair<4, 8>(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, tmem_base + Cfg::kColDK,
+        issue_pv_pair<2, 4>(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, tmem_base + Cfg::kColDK,
+                            tmem_base + Cfg::kColDPT, q_s, false);
+        ok = mbar_wait_hint(bar(Cfg::kBarPDSFull + 2), s & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv_pair<4, 6>(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, tmem_base + Cfg::kColDK,
+                            tmem_base + Cfg::kColDPT, q_s, false);
+        ok = mbar_wait_hint(bar(Cfg::kBarPDSFull + 3), s & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv_pair<6, 8>(tmem_base + Cfg::kColDV, tmem_base + Cfg::kColST, do_s, tmem_base + Cfg::kColDK,
                             tmem_base + Cfg::kColDPT, q_s, false);
         tc_commit(bar(Cfg::kBarQDEmpty + slot));
       }
@@ -564,17 +599,17 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       const float* vlse = reinterpret_cast<const float*>(smem + Cfg::kVecOff + slot * Cfg::kVecBytes);
       const float* vdl = vlse + 128;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sv[32], pv[32];
-        tmem_ld_16x256b_x8_pair_wait(tmem_base + Cfg::kColST + lane_off + 64u * half,
-                                     tmem_base + Cfg::kColDPT + lane_off + 64u * half, sv, pv);
-        uint32_t pp[16], dd[16];
+      for (int qt = 0; qt < 4; ++qt) {                                 // query quarter: 32 query columns
+        uint32_t sv[16], pv[16];
+        tmem_ld_16x256b_x4_pair_wait(tmem_base + Cfg::kColST + lane_off + 32u * qt,
+                                     tmem_base + Cfg::kColDPT + lane_off + 32u * qt, sv, pv);
+        uint32_t pp[8], dd[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
+        for (int r = 0; r < 4; ++r) {
           float pA[2], pB[2], dA[2], dB[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int qc = 64 * half + 8 * r + 2 * u + e;            // query row within its tile
+            const int qc = 32 * qt + 8 * r + 2 * u + e;              // query row within its tile
             const float l2 = vlse[qc];
             const float dl = vdl[qc];
             pA[e] = (diag && rA > qc) ? 0.0f : ex2_approx(__fmaf_rn(__uint_as_float(sv[4 * r + e]), c, -l2));
@@ -587,13 +622,14 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
           dd[2 * r] = pack_bf16x2(dA[0], dA[1]);
           dd[2 * r + 1] = pack_bf16x2(dB[0], dB[1]);
         }
-        // bf16 pairs of query columns 64*half.. go to columns 32*half.. of the
-        // same buffers; those fp32 columns were read in half 0
-        tmem_st_16x128b_x8(tmem_base + Cfg::kColST + lane_off + 32u * half, pp);
-        tmem_st_16x128b_x8(tmem_base + Cfg::kColDPT + lane_off + 32u * half, dd);
+        // bf16 pairs of query columns 32*qt.. go to columns 16*qt.. of the
+        // same buffers; those fp32 columns were read in this quarter or an
+        // earlier one
+        tmem_st_16x128b_x4(tmem_base + Cfg::kColST + lane_off + 16u * qt, pp);
+        tmem_st_16x128b_x4(tmem_base + Cfg::kColDPT + lane_off + 16u * qt, dd);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(Cfg::kBarPDSFull + half));
+        mbar_arrive(bar(Cfg::kBarPDSFull + qt));
       }
     }
     if (ok) ok = mbar_wait(bar(Cfg::kBarDone), 0, abort_flag, args.err, kDevTimeoutMma);
