@@ -53,7 +53,7 @@ NCU_TRAFFIC = {
     "decode": {"bytes": 537.09e6 + 0.45e6, "sources": "9a0cb83ce5b66799",
                "profile": "profiles/launch_list_bench_full.md"},
     # one kb_attn_backward call: the delta, dq and dk/dv kernels together
-    "backward": {"bytes": 3830.31e6 + 773.74e6, "sources": "f4db4f5479dd4cf2",
+    "backward": {"bytes": 3831.92e6 + 774.62e6, "sources": "dd64db72c75205b3",
                  "profile": "profiles/launch_list_bench_full.md"},
 }
 KERNEL_SOURCES = {
@@ -466,11 +466,15 @@ def run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_att
     pre_sets = [([q, k, v], o), ([torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)], torch.empty_like(o))]
     dec_sets = [([qd, kd, vd], od),
                 ([torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)], torch.empty_like(od))]
+    pre_launch = lambda ins, out: kb_attn.prefill(ins[0], ins[1], ins[2], out=out)  # noqa: E731
+    dec_launch = lambda ins, out: kb_attn.decode(ins[0], ins[1], ins[2], DECODE_CTX, out=out)  # noqa: E731
+    # untimed warm-up of the same pipeline: the first copies out of freshly
+    # pinned host buffers are slower than the steady state
+    pipelined_e2e(2, [hq, hk, hv], pre_sets, ho, pre_launch)
+    pipelined_e2e(2, [hqd, hkd, hvd], dec_sets, hod, dec_launch)
     barrier(world, local)
-    pre_ms = pipelined_e2e(n, [hq, hk, hv], pre_sets, ho,
-                           lambda ins, out: kb_attn.prefill(ins[0], ins[1], ins[2], out=out))
-    dec_ms = pipelined_e2e(n, [hqd, hkd, hvd], dec_sets, hod,
-                           lambda ins, out: kb_attn.decode(ins[0], ins[1], ins[2], DECODE_CTX, out=out))
+    pre_ms = pipelined_e2e(n, [hq, hk, hv], pre_sets, ho, pre_launch)
+    dec_ms = pipelined_e2e(n, [hqd, hkd, hvd], dec_sets, hod, dec_launch)
     kb_attn.check_device_status()
     h2d_gbs, d2h_gbs = link_bandwidth([hq, hk, hv], pre_sets[1][0], ho[0], o)
     # the downloaded results are the kernels' results
