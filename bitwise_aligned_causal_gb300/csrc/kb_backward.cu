@@ -22,6 +22,8 @@
 //                        S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q
 // Every product uses the two forms of the forward: both operands K-major in
 // shared memory (issue_qk), or A from TMEM and B MN-major (issue_pv).
+#include <type_traits>
+
 #include "kb_contract.cuh"
 #include "kb_launch.h"
 
@@ -36,6 +38,26 @@ __device__ __forceinline__ void drain_wait_b(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity))
     if (global_timer_ns() - t0 > 50000000ull) break;
+}
+
+// P = 2^(s c - lse2) and dS = P (dP - delta) of two adjacent columns, as
+// packed f32x2 operations (the same IEEE operations, so the same bits, as the
+// scalar fma, subtraction and product): `nl` and `nd` hold -lse2 and -delta.
+// A masked P is zero before dS is formed, so its dS is a signed zero as in the
+// scalar form.  Both values go out as one bf16 pair each.
+template <bool kMask>
+__device__ __forceinline__ void p_ds_pair(uint32_t s0, uint32_t s1, uint32_t dp0, uint32_t dp1, float2 c2,
+                                          float2 nl, float2 nd, bool m0, bool m1, uint32_t& p_bf,
+                                          uint32_t& ds_bf) {
+  const float2 a = __ffma2_rn(make_float2(__uint_as_float(s0), __uint_as_float(s1)), c2, nl);
+  float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+  if (kMask) {
+    if (m0) pp.x = 0.0f;
+    if (m1) pp.y = 0.0f;
+  }
+  const float2 d = __fmul2_rn(pp, __fadd2_rn(make_float2(__uint_as_float(dp0), __uint_as_float(dp1)), nd));
+  p_bf = pack_bf16x2(pp.x, pp.y);
+  ds_bf = pack_bf16x2(d.x, d.y);
 }
 
 // Two independent products of the same shape, their K steps interleaved
@@ -309,7 +331,23 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     const float lseB = vB ? __fmul_rn(args.lse[row0 + iB], kLog2e) : 0.0f;
     const float dlA = vA ? args.delta[row0 + iA] : 0.0f;
     const float dlB = vB ? args.delta[row0 + iB] : 0.0f;
-    const float c = score_scale_log2();
+    const float2 c2 = make_float2(score_scale_log2(), score_scale_log2());
+    const float2 nlA = make_float2(-lseA, -lseA), nlB = make_float2(-lseB, -lseB);
+    const float2 ndA = make_float2(-dlA, -dlA), ndB = make_float2(-dlB, -dlB);
+    // the diagonal tile masks keys past the row; the others take no select
+    auto tile_ds = [&](auto diag_tag, const uint32_t (&sv)[32], const uint32_t (&pv)[32], int half,
+                       uint32_t (&ds)[32]) {
+      constexpr bool kDiag = decltype(diag_tag)::value;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int key = 64 * half + 8 * r + 2 * u;                   // keys key, key + 1 within the tile
+        uint32_t unused;
+        p_ds_pair<kDiag>(sv[4 * r], sv[4 * r + 1], pv[4 * r], pv[4 * r + 1], c2, nlA, ndA, key > rA, key + 1 > rA,
+                         unused, ds[2 * (8 * half + r)]);
+        p_ds_pair<kDiag>(sv[4 * r + 2], sv[4 * r + 3], pv[4 * r + 2], pv[4 * r + 3], c2, nlB, ndB, key > rB,
+                         key + 1 > rB, unused, ds[2 * (8 * half + r) + 1]);
+      }
+    };
     bool ok = !skip;
     for (int j = 0; j < n_kv && ok; ++j) {
       ok = mbar_wait_hint(bar(Cfg::kBarSFull), j & 1, abort_flag, args.err, kDevTimeoutMma);
@@ -326,26 +364,12 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
                                    sv0, pv0, sv1, pv1);
       tc_fence_before();
       mbar_arrive(bar(Cfg::kBarSFree));                              // S(j), dP(j) fully read
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const uint32_t* sv = half ? sv1 : sv0;
-        const uint32_t* pv = half ? pv1 : pv0;
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          float dsA[2], dsB[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int key = 64 * half + 8 * r + 2 * u + e;           // key within the tile
-            const float pA = (diag && key > rA) ? 0.0f
-                                                : ex2_approx(__fmaf_rn(__uint_as_float(sv[4 * r + e]), c, -lseA));
-            const float pB = (diag && key > rB) ? 0.0f
-                                                : ex2_approx(__fmaf_rn(__uint_as_float(sv[4 * r + 2 + e]), c, -lseB));
-            dsA[e] = __fmul_rn(pA, __fsub_rn(__uint_as_float(pv[4 * r + e]), dlA));
-            dsB[e] = __fmul_rn(pB, __fsub_rn(__uint_as_float(pv[4 * r + 2 + e]), dlB));
-          }
-          ds[2 * (8 * half + r)] = pack_bf16x2(dsA[0], dsA[1]);
-          ds[2 * (8 * half + r) + 1] = pack_bf16x2(dsB[0], dsB[1]);
-        }
+      if (diag) {
+        tile_ds(std::true_type{}, sv0, pv0, 0, ds);
+        tile_ds(std::true_type{}, sv1, pv1, 1, ds);
+      } else {
+        tile_ds(std::false_type{}, sv0, pv0, 0, ds);
+        tile_ds(std::false_type{}, sv1, pv1, 1, ds);
       }
       if (j > 0) {                                                   // dQ(j-1) has read dS(j-1)
         ok = mbar_wait(bar(Cfg::kBarDQDone), (j - 1) & 1, abort_flag, args.err, kDevTimeoutMma);
@@ -405,7 +429,7 @@ struct BwdKVCfg {
   static constexpr uint32_t kVOff = kTileBytes;
   static constexpr uint32_t kQOff = 2 * kTileBytes;                   // slot s: Q at kQOff + s*2*tile,
   static constexpr uint32_t kSlotBytes = 2 * kTileBytes;              //         dO right after it
-  static constexpr uint32_t kVecOff = kQOff + kStages * kSlotBytes;   // slot s: lse2[128], delta[128]
+  static constexpr uint32_t kVecOff = kQOff + kStages * kSlotBytes;   // slot s: -lse2[128], -delta[128]
   static constexpr uint32_t kVecBytes = 2 * 128 * 4;
   static constexpr uint32_t kBarOff = kVecOff + kStages * kVecBytes;
   static constexpr int kBarKV = 0;                                    // K(jt), V(jt) landed
@@ -509,8 +533,8 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                              bar(Cfg::kBarQDFull + slot), keep);
         }
         issued = s + 1;
-        // lse (base 2) and delta of the step's 128 query rows; rows past the
-        // sequence get lse2 = +inf, so their P (and dS) is exactly zero
+        // -lse (base 2) and -delta of the step's 128 query rows; rows past the
+        // sequence get -lse2 = -inf, so their P (and dS) is exactly zero
         float* vec = reinterpret_cast<float*>(smem + Cfg::kVecOff + slot * Cfg::kVecBytes);
         const size_t row0 = (static_cast<size_t>(b) * args.Hq + h) * static_cast<size_t>(args.S);
 #pragma unroll
@@ -518,8 +542,8 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
           const int q = 4 * lane + e;
           const int i = it * kTileRows + q;
           const bool valid = i < args.S;
-          vec[q] = valid ? __fmul_rn(args.lse[row0 + i], kLog2e) : __int_as_float(0x7F800000);
-          vec[128 + q] = valid ? args.delta[row0 + i] : 0.0f;
+          vec[q] = valid ? -__fmul_rn(args.lse[row0 + i], kLog2e) : __int_as_float(0xFF800000);
+          vec[128 + q] = valid ? -args.delta[row0 + i] : -0.0f;
         }
         mbar_arrive(bar(Cfg::kBarVecFull + slot));
       }
@@ -585,7 +609,23 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const int u = lane & 3;
     const int rA = lane_base + (lane >> 2);
     const int rB = rA + 8;
-    const float c = score_scale_log2();
+    const float2 c2 = make_float2(score_scale_log2(), score_scale_log2());
+    // one query quarter: the diagonal step masks keys past the query, the
+    // others take no select
+    auto quarter = [&](auto diag_tag, const uint32_t (&sv)[16], const uint32_t (&pv)[16], const float* vnl,
+                       const float* vnd, int qt, uint32_t (&pp)[8], uint32_t (&dd)[8]) {
+      constexpr bool kDiag = decltype(diag_tag)::value;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int qc = 32 * qt + 8 * r + 2 * u;                      // query rows qc, qc + 1 within their tile
+        const float2 nl = *reinterpret_cast<const float2*>(vnl + qc);
+        const float2 nd = *reinterpret_cast<const float2*>(vnd + qc);
+        p_ds_pair<kDiag>(sv[4 * r], sv[4 * r + 1], pv[4 * r], pv[4 * r + 1], c2, nl, nd, rA > qc, rA > qc + 1,
+                         pp[2 * r], dd[2 * r]);
+        p_ds_pair<kDiag>(sv[4 * r + 2], sv[4 * r + 3], pv[4 * r + 2], pv[4 * r + 3], c2, nl, nd, rB > qc,
+                         rB > qc + 1, pp[2 * r + 1], dd[2 * r + 1]);
+      }
+    };
     bool ok = !skip;
     for (int s = 0; s < n_steps && ok; ++s) {
       const int slot = s % Cfg::kStages;
@@ -596,32 +636,16 @@ kb_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* vlse = reinterpret_cast<const float*>(smem + Cfg::kVecOff + slot * Cfg::kVecBytes);
-      const float* vdl = vlse + 128;
+      const float* vnl = reinterpret_cast<const float*>(smem + Cfg::kVecOff + slot * Cfg::kVecBytes);
+      const float* vnd = vnl + 128;
 #pragma unroll
       for (int qt = 0; qt < 4; ++qt) {                                 // query quarter: 32 query columns
         uint32_t sv[16], pv[16];
         tmem_ld_16x256b_x4_pair_wait(tmem_base + Cfg::kColST + lane_off + 32u * qt,
                                      tmem_base + Cfg::kColDPT + lane_off + 32u * qt, sv, pv);
         uint32_t pp[8], dd[8];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          float pA[2], pB[2], dA[2], dB[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int qc = 32 * qt + 8 * r + 2 * u + e;              // query row within its tile
-            const float l2 = vlse[qc];
-            const float dl = vdl[qc];
-            pA[e] = (diag && rA > qc) ? 0.0f : ex2_approx(__fmaf_rn(__uint_as_float(sv[4 * r + e]), c, -l2));
-            pB[e] = (diag && rB > qc) ? 0.0f : ex2_approx(__fmaf_rn(__uint_as_float(sv[4 * r + 2 + e]), c, -l2));
-            dA[e] = __fmul_rn(pA[e], __fsub_rn(__uint_as_float(pv[4 * r + e]), dl));
-            dB[e] = __fmul_rn(pB[e], __fsub_rn(__uint_as_float(pv[4 * r + 2 + e]), dl));
-          }
-          pp[2 * r] = pack_bf16x2(pA[0], pA[1]);
-          pp[2 * r + 1] = pack_bf16x2(pB[0], pB[1]);
-          dd[2 * r] = pack_bf16x2(dA[0], dA[1]);
-          dd[2 * r + 1] = pack_bf16x2(dB[0], dB[1]);
-        }
+        if (diag) quarter(std::true_type{}, sv, pv, vnl, vnd, qt, pp, dd);
+        else quarter(std::false_type{}, sv, pv, vnl, vnd, qt, pp, dd);
         // bf16 pairs of query columns 32*qt.. go to columns 16*qt.. of the
         // same buffers; those fp32 columns were read in this quarter or an
         // earlier one
