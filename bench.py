@@ -53,7 +53,7 @@ NCU_TRAFFIC = {
     "decode": {"bytes": 537.09e6 + 0.45e6, "sources": "9a0cb83ce5b66799",
                "profile": "profiles/launch_list_bench_full.md"},
     # one kb_attn_backward call: the delta, dq and dk/dv kernels together
-    "backward": {"bytes": 3831.92e6 + 774.62e6, "sources": "dd64db72c75205b3",
+    "backward": {"bytes": 3831.32e6 + 774.18e6, "sources": "238c1c90eea3b514",
                  "profile": "profiles/launch_list_bench_full.md"},
 }
 KERNEL_SOURCES = {
@@ -473,8 +473,13 @@ def run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_att
     pipelined_e2e(2, [hq, hk, hv], pre_sets, ho, pre_launch)
     pipelined_e2e(2, [hqd, hkd, hvd], dec_sets, hod, dec_launch)
     barrier(world, local)
-    pre_ms = pipelined_e2e(n, [hq, hk, hv], pre_sets, ho, pre_launch)
-    dec_ms = pipelined_e2e(n, [hqd, hkd, hvd], dec_sets, hod, dec_launch)
+    # three runs of the pipeline, the median reported: the host side of the
+    # link is shared with the machine's other work, and a run where the
+    # upload and the download stop overlapping reads far lower than the rest
+    pre_runs = [pipelined_e2e(n, [hq, hk, hv], pre_sets, ho, pre_launch) for _ in range(3)]
+    dec_runs = [pipelined_e2e(n, [hqd, hkd, hvd], dec_sets, hod, dec_launch) for _ in range(3)]
+    pre_ms = sorted(pre_runs)[1]
+    dec_ms = sorted(dec_runs)[1]
     kb_attn.check_device_status()
     h2d_gbs, d2h_gbs = link_bandwidth([hq, hk, hv], pre_sets[1][0], ho[0], o)
     # the downloaded results are the kernels' results
@@ -486,6 +491,8 @@ def run_e2e(args, x, y, q, k, v, o, qd, kd, vd, od, stream, world, local, kb_att
     return {"value": aggregate(pf, world, e2e_pre_ms / 1e3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "decode_gbs": aggregate(db, world, e2e_dec_ms / 1e3) / 1e9, "steps": n,
+            "runs_ms": {"prefill": [round(t, 4) for t in pre_runs], "decode": [round(t, 4) for t in dec_runs]},
+            "of_runs": "median of three pipelined runs of `steps` steps",
             "copy_only_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs},
             "note": ("every step uploads its inputs from pinned host memory and downloads its output; "
                      "two buffer sets let one step's copies overlap the neighbouring step's kernels; "
