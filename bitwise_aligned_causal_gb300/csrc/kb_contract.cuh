@@ -294,6 +294,12 @@ __device__ __forceinline__ float fold_o(float o_acc, float o_seg, FoldScale f) {
   return __fmaf_rn(o_acc, f.a, __fmul_rn(o_seg, f.b));
 }
 
+// fold_o on two columns at once, as packed f32x2 operations (the same two
+// round-to-nearest operations per column, so the same bits).
+__device__ __forceinline__ float2 fold_o2(float2 o_acc, float2 o_seg, FoldScale f) {
+  return __ffma2_rn(o_acc, make_float2(f.a, f.a), __fmul2_rn(o_seg, make_float2(f.b, f.b)));
+}
+
 // C5 fold of one finished segment into a thread's share of the folded O, in
 // the register layout of two 16x256b.x8 TMEM loads (columns 0-63 and
 // 64-127): registers 4r, 4r+1 of each half belong to the thread's row A,
@@ -317,11 +323,17 @@ __device__ __forceinline__ void fold_segment_quad(uint32_t (&acc0)[32], uint32_t
   FoldScale fB = fA;
   if (kRowB) fB = fold_state(accB, segB);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < 32; i += 2) {                      // registers i, i+1 belong to the same row
     if (!kRowB && (i & 2)) continue;
     const FoldScale f = (i & 2) ? fB : fA;
-    acc0[i] = __float_as_uint(fold_o(__uint_as_float(acc0[i]), __uint_as_float(o0[i]), f));
-    acc1[i] = __float_as_uint(fold_o(__uint_as_float(acc1[i]), __uint_as_float(o1[i]), f));
+    const float2 r0 = fold_o2(make_float2(__uint_as_float(acc0[i]), __uint_as_float(acc0[i + 1])),
+                              make_float2(__uint_as_float(o0[i]), __uint_as_float(o0[i + 1])), f);
+    const float2 r1 = fold_o2(make_float2(__uint_as_float(acc1[i]), __uint_as_float(acc1[i + 1])),
+                              make_float2(__uint_as_float(o1[i]), __uint_as_float(o1[i + 1])), f);
+    acc0[i] = __float_as_uint(r0.x);
+    acc0[i + 1] = __float_as_uint(r0.y);
+    acc1[i] = __float_as_uint(r1.x);
+    acc1[i + 1] = __float_as_uint(r1.y);
   }
 }
 

@@ -506,8 +506,12 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
             } else {
               tmem_ld32_wait(oacc_tmem + c * 32u, oa);
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                oa[i] = __float_as_uint(fold_o(__uint_as_float(oa[i]), __uint_as_float(os[i]), f));
+              for (int i = 0; i < 32; i += 2) {
+                const float2 r2 = fold_o2(make_float2(__uint_as_float(oa[i]), __uint_as_float(oa[i + 1])),
+                                          make_float2(__uint_as_float(os[i]), __uint_as_float(os[i + 1])), f);
+                oa[i] = __float_as_uint(r2.x);
+                oa[i + 1] = __float_as_uint(r2.y);
+              }
             }
             tmem_st32(oacc_tmem + c * 32u, oa);
           }
@@ -560,7 +564,12 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
           uint32_t oa[32];
           tmem_ld32_wait(oacc_tmem + c * 32u, oa);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(fold_o(__uint_as_float(oa[i]), __uint_as_float(o[i]), f));
+          for (int i = 0; i < 32; i += 2) {
+            const float2 r2 = fold_o2(make_float2(__uint_as_float(oa[i]), __uint_as_float(oa[i + 1])),
+                                      make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), f);
+            o[i] = __float_as_uint(r2.x);
+            o[i + 1] = __float_as_uint(r2.y);
+          }
         }
         normalise32(o, inv_l, w);
         if (store) {
@@ -747,15 +756,18 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         }
       };
       // the same arithmetic as fold_segment_quad on row A: fold_state, then
-      // fold_o on each of the thread's 32 columns
+      // fold_o2 on each pair of the thread's 32 columns
       auto fold_seg = [&](const float4& sv, const float2 (&ov)[16]) {
         const FoldScale f = fold_state(acc, RowState{sv.x, sv.y, sv.z});
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          acc0[4 * q] = __float_as_uint(fold_o(__uint_as_float(acc0[4 * q]), ov[q].x, f));
-          acc0[4 * q + 1] = __float_as_uint(fold_o(__uint_as_float(acc0[4 * q + 1]), ov[q].y, f));
-          acc1[4 * q] = __float_as_uint(fold_o(__uint_as_float(acc1[4 * q]), ov[8 + q].x, f));
-          acc1[4 * q + 1] = __float_as_uint(fold_o(__uint_as_float(acc1[4 * q + 1]), ov[8 + q].y, f));
+          const float2 r0 = fold_o2(make_float2(__uint_as_float(acc0[4 * q]), __uint_as_float(acc0[4 * q + 1])), ov[q], f);
+          const float2 r1 =
+              fold_o2(make_float2(__uint_as_float(acc1[4 * q]), __uint_as_float(acc1[4 * q + 1])), ov[8 + q], f);
+          acc0[4 * q] = __float_as_uint(r0.x);
+          acc0[4 * q + 1] = __float_as_uint(r0.y);
+          acc1[4 * q] = __float_as_uint(r1.x);
+          acc1[4 * q + 1] = __float_as_uint(r1.y);
         }
       };
       float4 svA, svB;
@@ -913,7 +925,11 @@ kb_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_consta
         const FoldScale f = fold_state(acc, RowState{cst.x, cst.y, cst.z});
         const float os[8] = {coa.x, coa.y, coa.z, coa.w, cob.x, cob.y, cob.z, cob.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = fold_o(o[i], os[i], f);
+        for (int i = 0; i < 8; i += 2) {
+          const float2 r2 = fold_o2(make_float2(o[i], o[i + 1]), make_float2(os[i], os[i + 1]), f);
+          o[i] = r2.x;
+          o[i + 1] = r2.y;
+        }
       }
       const float inv_l = row_inv_l(acc);
       const int head = r / Lc;

@@ -162,6 +162,17 @@ __device__ __forceinline__ bool unit_of(int p, int second, const PrefillArgs& ar
   return true;
 }
 
+// C5 fold of 16 columns of a segment's O into the folded O (columns base..).
+__device__ __forceinline__ void fold_chunk(uint32_t (&oacc)[128], int base, const uint32_t (&o)[16], FoldScale f) {
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const float2 r = fold_o2(make_float2(__uint_as_float(oacc[base + i]), __uint_as_float(oacc[base + i + 1])),
+                             make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), f);
+    oacc[base + i] = __float_as_uint(r.x);
+    oacc[base + i + 1] = __float_as_uint(r.y);
+  }
+}
+
 // The item a CTA runs at its step k: blockIdx.x + k * gridDim.x, or for the
 // snake every odd step from the other end.
 __device__ __forceinline__ int item_at(int k, const PrefillArgs& args) {
@@ -262,15 +273,10 @@ kb_prefill_kernel_s2(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
           for (int q = 0; q < 8; q += 2) {
             tmem_ld16_wait_for(oa);
             tmem_ld16_issue(o_tmem + 16u * (q + 1), ob);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              oacc[16 * q + i] = __float_as_uint(fold_o(__uint_as_float(oacc[16 * q + i]), __uint_as_float(oa[i]), f));
+            fold_chunk(oacc, 16 * q, oa, f);
             tmem_ld16_wait_for(ob);
             if (q + 2 < 8) tmem_ld16_issue(o_tmem + 16u * (q + 2), oa);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              oacc[16 * (q + 1) + i] =
-                  __float_as_uint(fold_o(__uint_as_float(oacc[16 * (q + 1) + i]), __uint_as_float(ob[i]), f));
+            fold_chunk(oacc, 16 * (q + 1), ob, f);
           }
         }
         tc_fence_before();
