@@ -48,12 +48,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the sources differ from that hash, the figure no longer describes the timed
 # build and the bench line reports traffic as null.
 NCU_TRAFFIC = {
-    "prefill": {"bytes": 806.23e6 + 503.38e6, "sources": "fc78aae055077c17",
+    "prefill": {"bytes": 806.31e6 + 503.93e6, "sources": "9ffdbcc262b023f9",
                 "profile": "profiles/launch_list_bench_full.md"},
-    "decode": {"bytes": 537.09e6 + 0.45e6, "sources": "9a0cb83ce5b66799",
+    "decode": {"bytes": 537.09e6 + 0.22e6, "sources": "fcbe3f1dc60b9ee3",
                "profile": "profiles/launch_list_bench_full.md"},
     # one kb_attn_backward call: the delta, dq and dk/dv kernels together
-    "backward": {"bytes": 3831.32e6 + 774.18e6, "sources": "238c1c90eea3b514",
+    "backward": {"bytes": 3832.81e6 + 774.76e6, "sources": "ceda1195f3bb5a52",
                  "profile": "profiles/launch_list_bench_full.md"},
 }
 KERNEL_SOURCES = {
