@@ -160,11 +160,12 @@ struct BwdQCfg {
   static constexpr int kBarVFull = kBarKEmpty + kKStages;  // 2: V(j) landed in slot j%2
   static constexpr int kBarVEmpty = kBarVFull + kVStages;  // 2: S(j), dP(j) done, V slot j%2 free
   static constexpr int kBarSFull = kBarVEmpty + kVStages;  // S(j), dP(j) in TMEM
-  static constexpr int kBarSFree = kBarSFull + 1;          // S(j), dP(j) read (256 arrivals)
+  static constexpr int kBarSFree = kBarSFull + 1;          // S(j) read (256 arrivals)
   static constexpr int kBarDSFull = kBarSFree + 1;         // dS(j) in TMEM (256 arrivals)
   static constexpr int kBarDQDone = kBarDSFull + 1;        // dQ += dS(j) K(j) finished
   static constexpr int kBarDrain = kBarDQDone + 1;          // 2: one per issuer
-  static constexpr int kNumBars = kBarDrain + 2;
+  static constexpr int kBarDPFree = kBarDrain + 2;         // dP(j) read (256 arrivals)
+  static constexpr int kNumBars = kBarDPFree + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -212,7 +213,7 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::kNumBars; ++i)
-      mbar_init(bar(i), (i == Cfg::kBarSFree || i == Cfg::kBarDSFull) ? 256u : 1u);
+      mbar_init(bar(i), (i == Cfg::kBarSFree || i == Cfg::kBarDSFull || i == Cfg::kBarDPFree) ? 256u : 1u);
     misc[1] = (*reinterpret_cast<volatile uint32_t*>(args.err) != 0) ? 1u : 0u;
     fence_mbar_init();
   }
@@ -282,8 +283,22 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
         if (ok && j > 0) ok = mbar_wait_hint(bar(Cfg::kBarSFree), (j - 1) & 1, abort_flag, args.err, kDevTimeoutSoftmax);
         if (!ok) break;
         tc_fence_after();
-        issue_qk_pair(tmem_base + Cfg::kColS, q_s, sbase + Cfg::kKOff + ks * kTileBytes,
-                      tmem_base + Cfg::kColDP, do_s, sbase + Cfg::kVOff + vs * kTileBytes);
+        // S's first K step goes out once S(j-1) has been read, the rest, with
+        // dP's steps interleaved, once dP(j-1) has been read too
+        const uint32_t k_s = sbase + Cfg::kKOff + ks * kTileBytes, v_s = sbase + Cfg::kVOff + vs * kTileBytes;
+        mma_ss(tmem_base + Cfg::kColS, desc_kmajor(q_s, 0, 1024u, kSlabBytes), desc_kmajor(k_s, 0, 1024u, kSlabBytes),
+               kIdescQK, 0u);
+        if (j > 0) ok = mbar_wait_hint(bar(Cfg::kBarDPFree), (j - 1) & 1, abort_flag, args.err, kDevTimeoutSoftmax);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_ss(tmem_base + Cfg::kColDP, desc_kmajor(do_s, kk, 1024u, kSlabBytes), desc_kmajor(v_s, kk, 1024u, kSlabBytes),
+                 kIdescQK, kk > 0 ? 1u : 0u);
+          if (kk < 7)
+            mma_ss(tmem_base + Cfg::kColS, desc_kmajor(q_s, kk + 1, 1024u, kSlabBytes),
+                   desc_kmajor(k_s, kk + 1, 1024u, kSlabBytes), kIdescQK, 1u);
+        }
         tc_commit(bar(Cfg::kBarSFull));
         tc_commit(bar(Cfg::kBarVEmpty + vs));
       }
@@ -358,12 +373,17 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       uint32_t ds[32];
       // all of S(j) and dP(j) into registers first, so S(j+1), dP(j+1) can be
       // issued while this tile's dS is computed
+      // S first, released on its own barrier, so S(j+1) can start while dP
+      // is still being read
       uint32_t sv0[32], pv0[32], sv1[32], pv1[32];
-      tmem_ld_16x256b_x8_quad_wait(tmem_base + Cfg::kColS + lane_off, tmem_base + Cfg::kColDP + lane_off,
-                                   tmem_base + Cfg::kColS + lane_off + 64u, tmem_base + Cfg::kColDP + lane_off + 64u,
-                                   sv0, pv0, sv1, pv1);
+      tmem_ld_16x256b_x8_pair_wait(tmem_base + Cfg::kColS + lane_off, tmem_base + Cfg::kColS + lane_off + 64u, sv0,
+                                   sv1);
       tc_fence_before();
-      mbar_arrive(bar(Cfg::kBarSFree));                              // S(j), dP(j) fully read
+      mbar_arrive(bar(Cfg::kBarSFree));                              // S(j) fully read
+      tmem_ld_16x256b_x8_pair_wait(tmem_base + Cfg::kColDP + lane_off, tmem_base + Cfg::kColDP + lane_off + 64u, pv0,
+                                   pv1);
+      tc_fence_before();
+      mbar_arrive(bar(Cfg::kBarDPFree));                             // dP(j) fully read
       if (diag) {
         tile_ds(std::true_type{}, sv0, pv0, 0, ds);
         tile_ds(std::true_type{}, sv1, pv1, 1, ds);
