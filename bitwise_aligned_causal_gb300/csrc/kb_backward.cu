@@ -165,7 +165,8 @@ struct BwdQCfg {
   static constexpr int kBarDQDone = kBarDSFull + 1;        // dQ += dS(j) K(j) finished
   static constexpr int kBarDrain = kBarDQDone + 1;          // 2: one per issuer
   static constexpr int kBarDPFree = kBarDrain + 2;         // dP(j) read (256 arrivals)
-  static constexpr int kNumBars = kBarDPFree + 1;
+  static constexpr int kBarSDone = kBarDPFree + 1;         // S(j) in TMEM (kBarSFull: dP(j) too)
+  static constexpr int kNumBars = kBarSDone + 1;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -298,6 +299,7 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
           if (kk < 7)
             mma_ss(tmem_base + Cfg::kColS, desc_kmajor(q_s, kk + 1, 1024u, kSlabBytes),
                    desc_kmajor(k_s, kk + 1, 1024u, kSlabBytes), kIdescQK, 1u);
+          if (kk == 6) tc_commit(bar(Cfg::kBarSDone));             // S is complete before dP's last step
         }
         tc_commit(bar(Cfg::kBarSFull));
         tc_commit(bar(Cfg::kBarVEmpty + vs));
@@ -365,21 +367,25 @@ kb_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     };
     bool ok = !skip;
     for (int j = 0; j < n_kv && ok; ++j) {
-      ok = mbar_wait_hint(bar(Cfg::kBarSFull), j & 1, abort_flag, args.err, kDevTimeoutMma);
+      ok = mbar_wait_hint(bar(Cfg::kBarSDone), j & 1, abort_flag, args.err, kDevTimeoutMma);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const bool diag = (j == n_kv - 1);
       uint32_t ds[32];
       // all of S(j) and dP(j) into registers first, so S(j+1), dP(j+1) can be
-      // issued while this tile's dS is computed
-      // S first, released on its own barrier, so S(j+1) can start while dP
-      // is still being read
+      // issued while this tile's dS is computed: S as soon as it is complete
+      // (before dP's last step), released on its own barrier so S(j+1) can
+      // start while dP is still being read
       uint32_t sv0[32], pv0[32], sv1[32], pv1[32];
       tmem_ld_16x256b_x8_pair_wait(tmem_base + Cfg::kColS + lane_off, tmem_base + Cfg::kColS + lane_off + 64u, sv0,
                                    sv1);
       tc_fence_before();
       mbar_arrive(bar(Cfg::kBarSFree));                              // S(j) fully read
+      ok = mbar_wait_hint(bar(Cfg::kBarSFull), j & 1, abort_flag, args.err, kDevTimeoutMma);   // dP(j) too
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
       tmem_ld_16x256b_x8_pair_wait(tmem_base + Cfg::kColDP + lane_off, tmem_base + Cfg::kColDP + lane_off + 64u, pv0,
                                    pv1);
       tc_fence_before();
