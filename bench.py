@@ -53,7 +53,7 @@ NCU_TRAFFIC = {
     "decode": {"bytes": 537.09e6 + 0.22e6, "sources": "fcbe3f1dc60b9ee3",
                "profile": "profiles/launch_list_bench_full.md"},
     # one kb_attn_backward call: the delta, dq and dk/dv kernels together
-    "backward": {"bytes": 3832.81e6 + 774.76e6, "sources": "ceda1195f3bb5a52",
+    "backward": {"bytes": 3832.15e6 + 774.73e6, "sources": "0195856a1fa6798b",
                  "profile": "profiles/launch_list_bench_full.md"},
 }
 KERNEL_SOURCES = {
